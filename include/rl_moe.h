@@ -1,0 +1,197 @@
+/*
+ * rl_moe.h - C ABI of the routed mixture-of-experts hot path on GB300 (sm_103a).
+ *
+ * The path, as the Red Lite engine notes describe it:
+ *   router  : f32 GEMV to expert logits, softmax top-k (candidates ordered by
+ *             logit, ties to the lower expert index), weights renormalised over
+ *             the selected experts, lookup of each selected expert in a
+ *             layers x experts residency table (slot address, 0 = absent), a
+ *             per-layer miss count and an early-out flag
+ *             ("Red Lite dev21 - GPU-routed decode (full residency)", section
+ *             "What changed": residency table, rl_route kernel;
+ *             "Red Lite dev23 - per-layer early-out and pre-gated expert
+ *             prefetch", section "What changed", item 1);
+ *   experts : gate/up/down projections of quantized experts with SwiGLU;
+ *   combine : each token's top-k outputs weighted and summed in router
+ *             selection order
+ *             ("Red Lite dev20 - batched prompt ingestion (native Metal
+ *             prefill)", section "What changed", items 2-3: (expert, token)
+ *             pairs sorted by expert, sum in selection order).
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless marked (host).  The caller allocates
+ *     and owns every buffer; the library keeps no pointer after a call returns
+ *     and never allocates, frees or synchronises.  Every call only enqueues
+ *     kernels on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ *     default stream).
+ *   - Arguments are validated on the host before any launch; on a bad
+ *     argument the call returns RL_ERR_INVALID (or RL_ERR_UNSUPPORTED for a
+ *     shape outside the supported set) and launches nothing.  RL_ERR_CUDA
+ *     reports a launch failure.  rl_last_error() gives a message for the last
+ *     non-OK status of the calling thread.  Nothing aborts or prints.
+ *   - `ctrl` is a 2-word int32 device control block owned by the caller:
+ *       ctrl[0] = early-out layer, RL_NO_EARLY_OUT when no layer missed;
+ *       ctrl[1] = device error bits (RL_DEVERR_*), 0 when healthy.
+ *     The caller initialises it and reads it after synchronising.  rl_route at
+ *     layer l returns at once on the device when ctrl[0] < l; every other call
+ *     for layer l returns at once when ctrl[0] <= l.  Device-side problems
+ *     (misaligned slot, bounded wait that ran out) set a bit in ctrl[1] and
+ *     skip the affected work; they never trap.
+ *   - Quantized format: a matrix is stored flat and row-major as consecutive
+ *     66-byte blocks of 256 values: bytes 0-1 = fp16 scale d (little-endian),
+ *     then 32 groups of (uint8 index into the 256 x 8 int8 codebook, uint8
+ *     sign mask); value j of a group = d * codebook[idx][j] * (bit j of the
+ *     sign mask ? -1 : +1).  An expert record is [gate I x H | up I x H |
+ *     down H x I] back to back (rl_record_bytes), at a 16-byte aligned slot
+ *     address.  Expert output o = down(silu(gate x) * (up x)).
+ *   - Supported shapes: hidden in {256, 512, 1024, 2048}; inter in {128, 256,
+ *     512, 1024, 2048}; 1 <= top_k <= 16; top_k <= n_experts <= 512;
+ *     top_k * inter <= 16384; n_layers >= 1.
+ */
+#ifndef RL_MOE_H
+#define RL_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rl_status {
+    RL_OK = 0,
+    RL_ERR_INVALID = 1,     /* bad argument; nothing launched */
+    RL_ERR_UNSUPPORTED = 2, /* shape outside the supported set; nothing launched */
+    RL_ERR_CUDA = 3,        /* a kernel launch failed */
+    RL_ERR_TIMEOUT = 4      /* reserved for host-visible bounded-wait expiry */
+} rl_status;
+
+#define RL_NO_EARLY_OUT 0x7fffffff
+#define RL_ABI_VERSION 1
+
+/* device error bits in ctrl[1] */
+#define RL_DEVERR_SLOT_ALIGN 1   /* a non-zero slot address was not 16-byte aligned */
+#define RL_DEVERR_WAIT_TIMEOUT 2 /* a bounded on-chip wait ran out of iterations */
+#define RL_DEVERR_BAD_ID 4       /* an expert id outside [0, n_experts) was read */
+#define RL_DEVERR_MISSING 8      /* an expert kernel met a zero (absent) slot */
+
+/* (host) model shape, passed by pointer to every call */
+typedef struct rl_moe_shape {
+    int32_t hidden;    /* H: token width */
+    int32_t n_experts; /* E: routed experts per layer */
+    int32_t top_k;     /* K: experts selected per token */
+    int32_t inter;     /* I: expert intermediate width */
+    int32_t n_layers;  /* L: layers covered by the residency table */
+} rl_moe_shape;
+
+int32_t rl_abi_version(void);
+/* Message for the last non-OK status returned to the calling thread ("" if none). */
+const char *rl_last_error(void);
+/* Bytes of one expert record: 3 * hidden * inter / 256 * 66. 0 for an invalid shape. */
+size_t rl_record_bytes(const rl_moe_shape *shp);
+
+/*
+ * rl_rmsnorm - unit-gain RMSNorm of T rows of width H:
+ *   xn[t][h] = x[t][h] * r_t,  r_t = 1 / sqrt(mean_h(x[t][h]^2) + eps), computed in f32.
+ * x, xn: [T][H] f32 row-major, 16-byte aligned (may alias).  H a multiple of 128; T >= 0.
+ * The scale r_t is computed with one fixed summation order; rl_route and moe_decode compute
+ * the very same r_t when they normalise their input on the fly (norm_eps >= 0).
+ */
+rl_status rl_rmsnorm(const float *x, float *xn, int32_t T, int32_t H, float eps, void *stream);
+
+/*
+ * rl_route - router for T tokens of one layer ("Red Lite dev21", "What changed": rl_route).
+ *   xn = x (norm_eps < 0) or RMSNorm(x) with unit gain and that eps (norm_eps >= 0)
+ *   logits[t][e] = sum_h w_router[e][h] * xn[t][h] (+ bias[e])          f32
+ *   ids[t][0..K-1]: the K largest logits in descending order; equal values (-0.0 == +0.0)
+ *                   go to the lower expert index
+ *   weights[t][k] = exp(l_k - l_0) / sum_j exp(l_j - l_0) over the selection   f32
+ *   slots[t][k]   = residency[layer][ids[t][k]]   (0 = not resident)
+ *   miss[layer]  += number of (t, k) with slots[t][k] == 0   (atomic, exact)
+ *   if that number > 0: ctrl[0] = min(ctrl[0], layer)
+ *     ("Red Lite dev23", "What changed", item 1: the router raises the flag at layer f).
+ * xn [T][H] f32; w_router [E][H] f32 row-major; bias [E] f32 or NULL; residency
+ * [n_layers][E] uint64 slot addresses; ids int32 [T][K]; weights f32 [T][K]; slots uint64 [T][K];
+ * miss uint32 [n_layers] (accumulated; the caller zeroes it); logits_out f32 [T][E] or NULL.
+ * ws: scratch of rl_route_workspace_bytes(shp, T) bytes, 16-byte aligned; it must be
+ * zero-filled before its first use (it holds a completion counter that every call leaves at
+ * zero); calls that share a workspace must not overlap on the GPU.
+ * x, w_router: 16-byte aligned.  0 <= layer < n_layers, T >= 0.
+ */
+size_t rl_route_workspace_bytes(const rl_moe_shape *shp, int32_t T);
+rl_status rl_route(const rl_moe_shape *shp, int32_t layer, int32_t T, const float *x, float norm_eps,
+                   const float *w_router, const float *bias, const uint64_t *residency,
+                   int32_t *ids, float *weights, uint64_t *slots, uint32_t *miss, int32_t *ctrl,
+                   float *logits_out, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * rl_resolve_slots - slots[t][k] = residency[layer][ids[t][k]] for T tokens, with no miss
+ * counting and no early-out check: re-resolves a layer's slots after its missing experts
+ * were filled ("Red Lite dev23", "What changed", item 1: layer f's misses are loaded and
+ * run with the ids the GPU selected).  ids int32 [T][K], slots uint64 [T][K].
+ */
+rl_status rl_resolve_slots(const rl_moe_shape *shp, int32_t layer, int32_t T, const int32_t *ids,
+                           const uint64_t *residency, uint64_t *slots, void *stream);
+
+/*
+ * moe_decode - routed experts of ONE token ("Red Lite dev21", "What changed": the
+ * single-token expert kernels read the slot table and weights rl_route wrote):
+ *   y[h] = (accumulate ? y[h] : 0) + sum_{k=0..K-1, in order} weights[k] * o_k[h],
+ *   o_k = down_k(silu(gate_k xn) * (up_k xn)), expert k at slots[k],
+ *   xn = x (norm_eps < 0) or RMSNorm(x) with unit gain and that eps (norm_eps >= 0).
+ * f32 CUDA-core arithmetic.  x [H] f32 (16-byte aligned); slots uint64 [K]; weights f32 [K];
+ * codebook int8 [256][8]; y [H] f32 (accumulate = 1 adds into y, e.g. the residual stream;
+ * y may be x); skip when ctrl[0] <= layer.
+ * A zero slot sets RL_DEVERR_MISSING and leaves y unchanged.
+ * ws: scratch of moe_decode_workspace_bytes(shp) bytes (K * inter f32 for h).
+ */
+size_t moe_decode_workspace_bytes(const rl_moe_shape *shp);
+rl_status moe_decode(const rl_moe_shape *shp, int32_t layer, const float *x, float norm_eps, const uint64_t *slots,
+                     const float *weights, const int8_t *codebook, float *y, int32_t accumulate,
+                     int32_t *ctrl, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * rl_build_pairs - (expert, token) pairs sorted by expert, stable in (t, k) order
+ * ("Red Lite dev20", "What changed", item 3):
+ *   offs[e] .. offs[e+1]-1 index the pairs of expert e; pair p is (pair_tok[p], pair_k[p]).
+ * ids int32 [T][K]; offs uint32 [E+1]; pair_tok uint32 [T*K]; pair_k uint8 [T*K].
+ * Skip when ctrl[0] <= layer.  ws: rl_build_pairs_workspace_bytes(shp, T) bytes (0 today).
+ */
+size_t rl_build_pairs_workspace_bytes(const rl_moe_shape *shp, int32_t T);
+rl_status rl_build_pairs(const rl_moe_shape *shp, int32_t layer, int32_t T, const int32_t *ids,
+                         uint32_t *offs, uint32_t *pair_tok, uint8_t *pair_k, int32_t *ctrl,
+                         void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_prefill_chunk - routed experts of a chunk of T tokens over the expert-sorted pairs
+ * ("Red Lite dev20", "What changed", item 3: batched gate/up and down over the pairs, then
+ * each token's top-k accumulated in router selection order):
+ *   y[t][h] = (accumulate ? y[t][h] : 0) + sum_{k in order} weights[t][k] * o_{t,k}[h].
+ * Gate/up and down run as grouped GEMMs on the 5th-generation tensor cores (tcgen05,
+ * accumulators in tensor memory) with both operands rounded to bf16 and f32 accumulation.
+ * xn [T][H] f32; offs/pair_tok/pair_k from rl_build_pairs; slots uint64 [T][K] and weights
+ * f32 [T][K] from rl_route; codebook int8 [256][8]; y [T][H] f32.  Skip when
+ * ctrl[0] <= layer.  ws: moe_prefill_workspace_bytes(shp, T) bytes.
+ */
+size_t moe_prefill_workspace_bytes(const rl_moe_shape *shp, int32_t T);
+rl_status moe_prefill_chunk(const rl_moe_shape *shp, int32_t layer, int32_t T, const float *xn,
+                            const uint32_t *offs, const uint32_t *pair_tok, const uint8_t *pair_k,
+                            const uint64_t *slots, const float *weights, const int8_t *codebook,
+                            float *y, int32_t accumulate, int32_t *ctrl, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/*
+ * moe_prefill_chunk_f32 - the same computation as moe_prefill_chunk with f32 CUDA-core
+ * arithmetic throughout (a cross-check of the grouped path at f32 accuracy).  Same
+ * arguments; ws: moe_prefill_workspace_bytes(shp, T) bytes.
+ */
+rl_status moe_prefill_chunk_f32(const rl_moe_shape *shp, int32_t layer, int32_t T, const float *xn,
+                                const uint32_t *offs, const uint32_t *pair_tok, const uint8_t *pair_k,
+                                const uint64_t *slots, const float *weights, const int8_t *codebook,
+                                float *y, int32_t accumulate, int32_t *ctrl, void *ws,
+                                size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RL_MOE_H */

@@ -1,0 +1,43 @@
+// prefill_common.cuh - argument checks, workspace layout and the ordered combine shared by
+// the two grouped prefill paths (tensor-core bf16 and CUDA-core f32).
+#pragma once
+#include "rl_common.cuh"
+
+namespace rl {
+
+struct PrefillArgs {
+    int layer, T, H, E, K, I, P, accumulate;
+    const float *xn;
+    const uint32_t *offs, *pair_tok;
+    const uint8_t *pair_k;
+    const uint64_t *slots;
+    const float *weights;
+    const int8_t *codebook;
+    float *y;
+    int32_t *ctrl;
+    // workspace carve-up
+    float *hbuf;              // [P][I]   f32 SwiGLU activations, pair order
+    float *outbuf;            // [T*K][H] f32 expert outputs, indexed by (token, k)
+    __nv_bfloat16 *xb;        // [T][H]   bf16 copy of xn (tensor-core path)
+    __nv_bfloat16 *hb;        // [P][I]   bf16 activations (tensor-core path)
+};
+
+struct PrefillWs {
+    size_t h, out, xb, hb, total;
+    PrefillWs(int T, int H, int K, int I) {
+        const size_t P = (size_t)T * K;
+        h = align_up(P * I * sizeof(float), 256);
+        out = align_up(P * H * sizeof(float), 256);
+        xb = align_up((size_t)T * H * 2, 256);
+        hb = align_up(P * I * 2, 256);
+        total = h + out + xb + hb;
+    }
+};
+
+rl_status prefill_check(const rl_moe_shape *shp, int32_t layer, int32_t T, const float *xn, const uint32_t *offs,
+                        const uint32_t *pair_tok, const uint8_t *pair_k, const uint64_t *slots,
+                        const float *weights, const int8_t *codebook, float *y, int32_t accumulate,
+                        int32_t *ctrl, void *ws, size_t ws_bytes, const char *who, PrefillArgs *a);
+rl_status launch_ordered_sum(const PrefillArgs &a, cudaStream_t s);
+
+}  // namespace rl

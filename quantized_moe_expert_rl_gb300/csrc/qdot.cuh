@@ -1,0 +1,99 @@
+// qdot.cuh - in-register decode of the 66-byte codebook blocks for the CUDA-core GEMVs.
+//
+// The 256 x 8 int8 codebook is converted once per CTA into a table of bf16 pairs (every
+// int8 value is exact in bf16): entry idx = 4 words, word i = bf16(g[2i]) | bf16(g[2i+1]) << 16.
+// The table is stored 8 times, interleaved so that entry e of copy c sits at 16-byte slot
+// e*8 + c; lane L reads copy L & 7, so the 8 lanes of each quarter-warp phase of a 128-bit
+// shared load always hit 8 different bank quads, whatever indices they look up.
+//
+// Signs: for sign byte s, s2 = s | (bits 1..7 of s moved to bits 16..22); then
+// (s2 << (15 - 2i)) has bit 2i of s at bit 15 and bit 2i+1 at bit 31, exactly the bf16 sign
+// bits of word i, so one shift and one LOP3 sign a pair.  The two bf16 halves become f32 by
+// a shift (low) and a mask (high), and a packed f32x2 FMA accumulates both.
+#pragma once
+#include "rl_common.cuh"
+
+namespace rl {
+
+constexpr int kTabCopies = 8;
+constexpr int kTabBytes = 256 * 16 * kTabCopies;  // 32 KB
+
+__device__ __forceinline__ uint32_t bf16_bits(int v) {
+    // exact for |v| <= 256: bf16 has an 8-bit significand
+    return __float_as_uint((float)v) >> 16;
+}
+
+// Build the replicated pair table from the int8 codebook with the whole CTA.  The 2 KB
+// codebook is first staged through `stage` (>= 2 KB of shared memory, reused afterwards) with
+// one coalesced load per thread, then expanded; ends with __syncthreads().
+__device__ __forceinline__ void build_pair_table(uint4 *tab, const int8_t *__restrict__ codebook, uint2 *stage) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) stage[i] = reinterpret_cast<const uint2 *>(codebook)[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256 * kTabCopies; i += blockDim.x) {
+        const int e = i / kTabCopies;
+        const uint2 raw = stage[e];
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t word = p < 2 ? raw.x : raw.y;
+            const int g0 = (int8_t)((word >> (16 * (p & 1))) & 0xffu);
+            const int g1 = (int8_t)((word >> (16 * (p & 1) + 8)) & 0xffu);
+            w[p] = bf16_bits(g0) | (bf16_bits(g1) << 16);
+        }
+        tab[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
+    return (unsigned long long)lo | ((unsigned long long)hi << 32);
+}
+__device__ __forceinline__ float hsum2(unsigned long long a) {
+    return __uint_as_float((uint32_t)a) + __uint_as_float((uint32_t)(a >> 32));
+}
+
+// One signed bf16 pair word -> packed (lo, hi) f32 pair.
+__device__ __forceinline__ unsigned long long signed_pair(uint32_t w, uint32_t s2, int shift) {
+    const uint32_t ws = w ^ ((s2 << shift) & 0x80008000u);
+    return pack2(ws << 16, ws & 0xffff0000u);
+}
+
+// acc += sum_{j<8} grid[idx][j] * (+-1)_j * x[j] for one group; `gs` = (idx | sign << 8),
+// `x` = 4 packed f32 pairs (x0,x1) (x2,x3) (x4,x5) (x6,x7), `tabc` = this lane's table copy.
+__device__ __forceinline__ unsigned long long group_fma(uint32_t gs, const unsigned long long *x,
+                                                        const uint4 *tabc, unsigned long long acc) {
+    const uint4 q = tabc[(gs & 0xffu) * kTabCopies];
+    const uint32_t s = (gs >> 8) & 0xffu;
+    const uint32_t s2 = s | ((s << 15) & 0x007f0000u);
+    acc = ffma2(signed_pair(q.x, s2, 15), x[0], acc);
+    acc = ffma2(signed_pair(q.y, s2, 13), x[1], acc);
+    acc = ffma2(signed_pair(q.z, s2, 11), x[2], acc);
+    acc = ffma2(signed_pair(q.w, s2, 9), x[3], acc);
+    return acc;
+}
+
+// Deterministic RMSNorm scale 1/sqrt(mean(x^2) + eps) of H values, computed by ONE warp with a
+// fixed summation order (identical in every kernel that calls it, so every kernel sees the
+// same normalised input).  Returns the scale in every lane.
+__device__ __forceinline__ float rms_scale_warp(const float *__restrict__ x, int H, float eps) {
+    const int lane = threadIdx.x & 31;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int c = lane * 4; c < H; c += 128) {
+        const float4 v = *reinterpret_cast<const float4 *>(x + c);
+        a0 = fmaf(v.x, v.x, a0); a1 = fmaf(v.y, v.y, a1); a2 = fmaf(v.z, v.z, a2); a3 = fmaf(v.w, v.w, a3);
+    }
+    float ss = warp_sum((a0 + a1) + (a2 + a3));
+    return 1.0f / sqrtf(ss / (float)H + eps);
+}
+
+// ---- programmatic dependent launch ---------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+}  // namespace rl

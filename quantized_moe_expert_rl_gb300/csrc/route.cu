@@ -1,0 +1,382 @@
+// route.cu - RMSNorm, router logits (f32), top-k selection with renormalised weights,
+// residency lookup, per-layer miss count and early-out flag.
+//
+// Red Lite dev21 - GPU-routed decode (full residency), "What changed": rl_route selects the
+// top-k on the GPU by logit with ties to the lower index, renormalises the weights over the
+// selection, looks each expert up in the layers x experts residency table and writes the slot
+// table, the weights and a per-layer miss count.
+// Red Lite dev23 - per-layer early-out, "What changed" item 1: the router raises the flag at
+// the first layer that selects a non-resident expert; later kernels then return at once.
+//
+// One token (decode): one kernel.  Each CTA owns 4 router rows, which it moves into shared
+// memory with one bulk copy BEFORE griddepcontrol.wait (the router weights depend on nothing
+// the previous kernel writes), so the 4 MB of router weights stream in while the previous
+// layer finishes.  After the wait each warp dots one row with xn held in registers; the last
+// CTA to finish (completion counter) selects, looks up and writes the outputs.
+// Many tokens (prefill): f32 tiled GEMM, then one warp per token selects.
+#include "qdot.cuh"
+
+namespace rl {
+
+// ---------------------------------------------------------------------------------------------
+// Selection: one warp.  Lane l holds experts l*C .. l*C+C-1 (C = candidates per lane), so a
+// lower lane always holds lower expert indices.  Keys are the f32 logits mapped to
+// order-preserving uint32 after folding -0.0 into +0.0 (so the two compare equal); key 0 is
+// below every finite value and marks a taken or absent candidate.  Each round takes the warp
+// maximum with redux.sync; among equal keys the lowest lane wins, and inside a lane the first
+// (lowest) index wins, so ties go to the lower expert index.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t b = __float_as_uint(v + 0.0f);  // -0.0 + 0.0 = +0.0
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+template <int C>
+__device__ __forceinline__ void warp_select(const float *lg, const uint64_t *__restrict__ table_row,
+                                            int32_t *ids, float *weights, uint64_t *slots, uint32_t *miss_l,
+                                            int32_t *ctrl, int layer, int E, int K) {
+    const int lane = threadIdx.x & 31;
+    uint32_t key[C];
+    uint32_t best = 0u;
+    int bi = 0;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+        const int e = lane * C + i;
+        key[i] = e < E ? order_key(__ldcg(lg + e)) : 0u;
+        if (key[i] > best) { best = key[i]; bi = i; }
+    }
+    int my_id = 0;
+    float my_val = 0.f;
+    for (int r = 0; r < K; ++r) {
+        const uint32_t m = __reduce_max_sync(kFull, best);
+        const int wl = __ffs(__ballot_sync(kFull, best == m)) - 1;
+        const int wi = __shfl_sync(kFull, bi, wl);
+        if (lane == r) { my_id = wl * C + wi; my_val = key_value(m); }
+        if (lane == wl) {  // the winner drops its candidate and finds its next best
+            best = 0u;
+            bi = 0;
+#pragma unroll
+            for (int i = 0; i < C; ++i) {
+                if (i == wi) key[i] = 0u;
+                if (key[i] > best) { best = key[i]; bi = i; }
+            }
+        }
+    }
+    // w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0), the sum taken in selection order
+    const float l0 = __shfl_sync(kFull, my_val, 0);
+    const float ex = lane < K ? expf(my_val - l0) : 0.f;
+    float tot = 0.f;
+    for (int k = 0; k < K; ++k) tot += __shfl_sync(kFull, ex, k);
+    uint64_t slot = 1;
+    if (lane < K) {
+        ids[lane] = my_id;
+        weights[lane] = ex / tot;
+        slot = table_row[my_id];
+        slots[lane] = slot;
+    }
+    const int nmiss = __popc(__ballot_sync(kFull, lane < K && slot == 0));
+    if (lane == 0 && nmiss > 0) {
+        atomicAdd(miss_l, (uint32_t)nmiss);
+        atomicMin(ctrl, layer);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// RMSNorm: one CTA per token; warp 0 computes the deterministic scale, all threads apply it.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float *__restrict__ x, float *__restrict__ xn, int H,
+                                                      float eps) {
+    __shared__ float r_s;
+    const float *xr = x + (size_t)blockIdx.x * H;
+    if (threadIdx.x < 32) {
+        const float r = rms_scale_warp(xr, H, eps);
+        if (threadIdx.x == 0) r_s = r;
+    }
+    __syncthreads();
+    const float r = r_s;
+    float *yr = xn + (size_t)blockIdx.x * H;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) yr[i] = xr[i] * r;
+}
+
+// ---------------------------------------------------------------------------------------------
+// One token: fused RMSNorm (optional) + logits + last-CTA selection.
+// NV = H / 128 float4 columns per lane (lane l owns columns 4l + 128j, j < NV).
+// ---------------------------------------------------------------------------------------------
+constexpr int kR1Rows = 4;
+constexpr int kR1Threads = 32 * kR1Rows;
+
+template <int NV, bool NORM, int C>
+__global__ void __launch_bounds__(kR1Threads) route1_kernel(const float *__restrict__ x, float eps,
+                                                            const float *__restrict__ W,
+                                                            const float *__restrict__ bias,
+                                                            const uint64_t *__restrict__ table_row, int32_t *ids,
+                                                            float *weights, uint64_t *slots, uint32_t *miss_l,
+                                                            int32_t *ctrl, int layer, float *logits,
+                                                            unsigned *counter, int E, int K) {
+    constexpr int H = NV * 128;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    float *scale_s = reinterpret_cast<float *>(smem + 16);
+    int *last_s = reinterpret_cast<int *>(smem + 20);
+    float *Ws = reinterpret_cast<float *>(smem + 128);  // [kR1Rows][H]
+    const int e0 = blockIdx.x * kR1Rows, nr = min(kR1Rows, E - e0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        const uint32_t bytes = (uint32_t)(nr * H * sizeof(float));
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(Ws, W + (size_t)e0 * H, bytes, bar);
+    }
+    __syncthreads();
+    pdl_wait();
+    const bool skip = ld_ctrl(ctrl) < layer;
+    float4 xv[NV];
+    if (!skip) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) xv[j] = reinterpret_cast<const float4 *>(x)[lane + 32 * j];
+        if (NORM && warp == 0) {
+            const float r = rms_scale_warp(x, H, eps);
+            if (lane == 0) *scale_s = r;
+        }
+    }
+    __syncthreads();
+    // the router rows must have landed before the CTA may exit, whether it skips or not
+    if (!mbar_wait(bar, 0)) {
+        if (threadIdx.x == 0) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
+        return;
+    }
+    if (skip) return;
+    pdl_trigger();
+    if (warp < nr) {
+        const float r = NORM ? *scale_s : 1.f;
+        const float4 *wr = reinterpret_cast<const float4 *>(Ws + warp * H);
+        unsigned long long a0 = 0, a1 = 0;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            float4 v = xv[j];
+            if (NORM) { v.x *= r; v.y *= r; v.z *= r; v.w *= r; }
+            const float4 w = wr[lane + 32 * j];
+            a0 = ffma2(pack2(__float_as_uint(w.x), __float_as_uint(w.y)),
+                       pack2(__float_as_uint(v.x), __float_as_uint(v.y)), a0);
+            a1 = ffma2(pack2(__float_as_uint(w.z), __float_as_uint(w.w)),
+                       pack2(__float_as_uint(v.z), __float_as_uint(v.w)), a1);
+        }
+        const float s = warp_sum(hsum2(a0) + hsum2(a1));
+        if (lane == 0) logits[e0 + warp] = s + (bias ? bias[e0 + warp] : 0.f);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(counter, 1u);
+        *last_s = prev == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!*last_s) return;
+    __threadfence();
+    if (warp == 0) {
+        warp_select<C>(logits, table_row, ids, weights, slots, miss_l, ctrl, layer, E, K);
+        if (lane == 0) *counter = 0u;  // every call leaves the counter at zero
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Many tokens: 64 x 64 (tokens x experts) tiles, K step 16, 4 x 4 outputs per thread.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) router_gemm_kernel(const float *__restrict__ xn, const float *__restrict__ W,
+                                                          const float *__restrict__ bias,
+                                                          float *__restrict__ logits, int T, int H, int E,
+                                                          const int32_t *ctrl, int layer) {
+    if (ld_ctrl(ctrl) < layer) return;
+    __shared__ float As[16][68];
+    __shared__ float Bs[16][68];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int t_base = blockIdx.y * 64, e_base = blockIdx.x * 64;
+    const int lrow = tid >> 2, lk = (tid & 3) * 4;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < H; k0 += 16) {
+        {
+            const int t = t_base + lrow;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < T) v = *reinterpret_cast<const float4 *>(xn + (size_t)t * H + k0 + lk);
+            As[lk + 0][lrow] = v.x; As[lk + 1][lrow] = v.y; As[lk + 2][lrow] = v.z; As[lk + 3][lrow] = v.w;
+            const int e = e_base + lrow;
+            float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < E) w = *reinterpret_cast<const float4 *>(W + (size_t)e * H + k0 + lk);
+            Bs[lk + 0][lrow] = w.x; Bs[lk + 1][lrow] = w.y; Bs[lk + 2][lrow] = w.z; Bs[lk + 3][lrow] = w.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t_base + ty + 16 * i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e_base + tx + 16 * j;
+            if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+        }
+    }
+}
+
+template <int C>
+__global__ void __launch_bounds__(256) route_select_kernel(const float *__restrict__ logits,
+                                                           const uint64_t *__restrict__ table_row, int32_t *ids,
+                                                           float *weights, uint64_t *slots, uint32_t *miss_l,
+                                                           int32_t *ctrl, int layer, int T, int E, int K) {
+    if (ld_ctrl(ctrl) < layer) return;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const size_t o = (size_t)t * K;
+    warp_select<C>(logits + (size_t)t * E, table_row, ids + o, weights + o, slots + o, miss_l, ctrl, layer, E, K);
+}
+
+__global__ void resolve_slots_kernel(const int32_t *__restrict__ ids, const uint64_t *__restrict__ table_row,
+                                     uint64_t *__restrict__ slots, int n, int E) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int e = ids[i];
+    slots[i] = (e >= 0 && e < E) ? table_row[e] : 0;
+}
+
+struct RouteWs {  // [counter (256 B) | logits T*E f32 | normalised input T*H f32 (T > 1 with norm)]
+    size_t logits, xn, total;
+    RouteWs(int T, int E, int H, bool norm) {
+        logits = 256;
+        xn = logits + align_up((size_t)T * E * sizeof(float), 256);
+        total = xn + (norm && T > 1 ? align_up((size_t)T * H * sizeof(float), 256) : 0);
+    }
+};
+
+template <int NV, bool NORM>
+static rl_status launch_route1(const float *x, float eps, const float *W, const float *bias, const uint64_t *row,
+                               int32_t *ids, float *w, uint64_t *slots, uint32_t *miss_l, int32_t *ctrl, int layer,
+                               float *logits, unsigned *counter, int E, int K, cudaStream_t s) {
+    const size_t sm = 128 + (size_t)kR1Rows * NV * 128 * sizeof(float);
+    const dim3 g((E + kR1Rows - 1) / kR1Rows), b(kR1Threads);
+#define RL_R1(C)                                                                                                     \
+    return launch_pdl(route1_kernel<NV, NORM, C>, g, b, sm, s, "rl_route", x, eps, W, bias, row, ids, w, slots,     \
+                      miss_l, ctrl, layer, logits, counter, E, K)
+    if (E <= 32) RL_R1(1);
+    if (E <= 64) RL_R1(2);
+    if (E <= 128) RL_R1(4);
+    if (E <= 256) RL_R1(8);
+    RL_R1(16);
+#undef RL_R1
+}
+
+template <int NV>
+static rl_status launch_route1_n(bool norm, const float *x, float eps, const float *W, const float *bias,
+                                 const uint64_t *row, int32_t *ids, float *w, uint64_t *slots, uint32_t *miss_l,
+                                 int32_t *ctrl, int layer, float *logits, unsigned *counter, int E, int K,
+                                 cudaStream_t s) {
+    if (norm)
+        return launch_route1<NV, true>(x, eps, W, bias, row, ids, w, slots, miss_l, ctrl, layer, logits, counter, E,
+                                       K, s);
+    return launch_route1<NV, false>(x, eps, W, bias, row, ids, w, slots, miss_l, ctrl, layer, logits, counter, E, K,
+                                    s);
+}
+
+}  // namespace rl
+
+using namespace rl;
+
+extern "C" rl_status rl_rmsnorm(const float *x, float *xn, int32_t T, int32_t H, float eps, void *stream) {
+    if (!x || !xn) return fail(RL_ERR_INVALID, "rl_rmsnorm: NULL buffer");
+    if (T < 0 || H <= 0 || (H % 128)) return fail(RL_ERR_INVALID, "rl_rmsnorm: bad T=%d or H=%d", T, H);
+    if (!(eps >= 0.f)) return fail(RL_ERR_INVALID, "rl_rmsnorm: eps must be >= 0");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xn)) & 15)
+        return fail(RL_ERR_INVALID, "rl_rmsnorm: buffers must be 16-byte aligned");
+    if (T == 0) return RL_OK;
+    rmsnorm_kernel<<<T, 256, 0, as_stream(stream)>>>(x, xn, H, eps);
+    return check_launch("rl_rmsnorm");
+}
+
+extern "C" size_t rl_route_workspace_bytes(const rl_moe_shape *shp, int32_t T) {
+    if (!shp || T < 0 || shp->n_experts <= 0 || shp->hidden <= 0) return 0;
+    return RouteWs(T, shp->n_experts, shp->hidden, true).total;
+}
+
+extern "C" rl_status rl_route(const rl_moe_shape *shp, int32_t layer, int32_t T, const float *x, float norm_eps,
+                              const float *w_router, const float *bias, const uint64_t *residency, int32_t *ids,
+                              float *weights, uint64_t *slots, uint32_t *miss, int32_t *ctrl, float *logits_out,
+                              void *ws, size_t ws_bytes, void *stream) {
+    rl_status st = check_shape(shp);
+    if (st != RL_OK) return st;
+    if (layer < 0 || layer >= shp->n_layers)
+        return fail(RL_ERR_INVALID, "rl_route: layer %d outside [0,%d)", layer, shp->n_layers);
+    if (T < 0) return fail(RL_ERR_INVALID, "rl_route: T=%d", T);
+    if (!x || !w_router || !residency || !ids || !weights || !slots || !miss || !ctrl)
+        return fail(RL_ERR_INVALID, "rl_route: NULL required buffer");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router) |
+         reinterpret_cast<uintptr_t>(ws)) & 15)
+        return fail(RL_ERR_INVALID, "rl_route: x, w_router and ws must be 16-byte aligned");
+    const int H = shp->hidden, E = shp->n_experts, K = shp->top_k;
+    const bool norm = norm_eps >= 0.f;
+    const RouteWs L(T, E, H, norm);
+    if (!ws || ws_bytes < L.total)
+        return fail(RL_ERR_INVALID, "rl_route: workspace of %zu B needed, %zu given", L.total, ws_bytes);
+    if (T == 0) return RL_OK;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    unsigned *counter = reinterpret_cast<unsigned *>(w8);
+    float *logits = logits_out ? logits_out : reinterpret_cast<float *>(w8 + L.logits);
+    const uint64_t *row = residency + (size_t)layer * E;
+    uint32_t *miss_l = miss + layer;
+    cudaStream_t s = as_stream(stream);
+    if (T == 1) {
+        switch (H) {
+            case 256: return launch_route1_n<2>(norm, x, norm_eps, w_router, bias, row, ids, weights, slots, miss_l,
+                                                ctrl, layer, logits, counter, E, K, s);
+            case 512: return launch_route1_n<4>(norm, x, norm_eps, w_router, bias, row, ids, weights, slots, miss_l,
+                                                ctrl, layer, logits, counter, E, K, s);
+            case 1024: return launch_route1_n<8>(norm, x, norm_eps, w_router, bias, row, ids, weights, slots, miss_l,
+                                                 ctrl, layer, logits, counter, E, K, s);
+            default: return launch_route1_n<16>(norm, x, norm_eps, w_router, bias, row, ids, weights, slots, miss_l,
+                                                ctrl, layer, logits, counter, E, K, s);
+        }
+    }
+    const float *src = x;
+    if (norm) {
+        float *xn = reinterpret_cast<float *>(w8 + L.xn);
+        rmsnorm_kernel<<<T, 256, 0, s>>>(x, xn, H, norm_eps);
+        src = xn;
+    }
+    router_gemm_kernel<<<dim3((E + 63) / 64, (T + 63) / 64), 256, 0, s>>>(src, w_router, bias, logits, T, H, E, ctrl,
+                                                                        layer);
+    const dim3 g((T + 7) / 8), b(256);
+    if (E <= 32) route_select_kernel<1><<<g, b, 0, s>>>(logits, row, ids, weights, slots, miss_l, ctrl, layer, T, E, K);
+    else if (E <= 64) route_select_kernel<2><<<g, b, 0, s>>>(logits, row, ids, weights, slots, miss_l, ctrl, layer, T, E, K);
+    else if (E <= 128) route_select_kernel<4><<<g, b, 0, s>>>(logits, row, ids, weights, slots, miss_l, ctrl, layer, T, E, K);
+    else if (E <= 256) route_select_kernel<8><<<g, b, 0, s>>>(logits, row, ids, weights, slots, miss_l, ctrl, layer, T, E, K);
+    else route_select_kernel<16><<<g, b, 0, s>>>(logits, row, ids, weights, slots, miss_l, ctrl, layer, T, E, K);
+    return check_launch("rl_route");
+}
+
+extern "C" rl_status rl_resolve_slots(const rl_moe_shape *shp, int32_t layer, int32_t T, const int32_t *ids,
+                                      const uint64_t *residency, uint64_t *slots, void *stream) {
+    rl_status st = check_shape(shp);
+    if (st != RL_OK) return st;
+    if (layer < 0 || layer >= shp->n_layers) return fail(RL_ERR_INVALID, "rl_resolve_slots: layer %d", layer);
+    if (T < 0 || !ids || !residency || !slots) return fail(RL_ERR_INVALID, "rl_resolve_slots: bad arguments");
+    const int n = T * shp->top_k;
+    if (n == 0) return RL_OK;
+    resolve_slots_kernel<<<(n + 255) / 256, 256, 0, as_stream(stream)>>>(
+        ids, residency + (size_t)layer * shp->n_experts, slots, n, shp->n_experts);
+    return check_launch("rl_resolve_slots");
+}

@@ -1,0 +1,321 @@
+"""Host-side drivers around the C ABI: the resident expert pool and residency table, the
+per-token decode chain (captured as one CUDA graph per token), the prefill chunk chain, and
+the bounded-residency chain with per-layer early-out, fill and resume.
+
+PyTorch is used here only for device memory, pinned host memory, streams, events and
+graphs.  Every step of the routed-MoE path runs in librlmoe's kernels.
+
+Early-out and resume follow "Red Lite dev23 - per-layer early-out and pre-gated expert
+prefetch", section "What changed", item 1: when layer f selects a non-resident expert the
+router raises the flag, later kernels return at once, the host loads only layer f's missing
+experts (here: copies their records from a pinned host backing store into free HBM slots and
+updates the residency table), runs layer f with the ids and weights the GPU selected, and
+resumes the chain at f + 1.  Nothing is evicted: the pool has a slot for every expert.
+"""
+from __future__ import annotations
+
+import time
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import _lib as L
+from ._lib import RL_NO_EARLY_OUT, RlShape
+
+EPS = 1e-6
+
+
+def shape_of(w) -> RlShape:
+    return RlShape.of(w.hidden, w.n_experts, w.top_k, w.inter, w.n_layers)
+
+
+class Model:
+    """A synthetic model resident on one GPU: codebook, routers (+ Zipf biases), the expert
+    pool (one record slot per (layer, expert)), the residency table and, for bounded
+    residency, a pinned host backing store of the absent experts' records."""
+
+    def __init__(self, w, device="cuda", slot_perm: bool = False, layers: int | None = None,
+                 gen_threads: int = 0):
+        import synth
+        self.w = w
+        self.L = w.n_layers if layers is None else layers
+        self.shape = RlShape.of(w.hidden, w.n_experts, w.top_k, w.inter, self.L)
+        self.device = torch.device(device)
+        E, H, rb = w.n_experts, w.hidden, w.record_bytes
+        self.record_bytes = rb
+        assert L.rl_record_bytes(self.shape) == rb
+        self.codebook = torch.from_numpy(synth.grid(w.seed).reshape(-1).copy()).to(self.device)
+        self.routers = torch.empty((self.L, E, H), dtype=torch.float32, device=self.device)
+        self.bias = None
+        if w.zipf_s > 0:
+            self.bias = torch.empty((self.L, E), dtype=torch.float32, device=self.device)
+        self.pool = torch.empty(self.L * E * rb, dtype=torch.uint8, device=self.device)
+        base = self.pool.data_ptr()
+        assert base % 256 == 0
+        # slot position of each (layer, expert) inside the pool
+        self.pos = np.empty((self.L, E), dtype=np.int64)
+        for l in range(self.L):
+            perm = synth.permutation(synth.TAG_SLOTPERM, l, E, w.seed) if slot_perm else np.arange(E)
+            self.pos[l] = l * E + perm
+        self.addr = (np.uint64(base) + self.pos.astype(np.uint64) * np.uint64(rb)).astype(np.uint64)
+        self.resident = np.ones((self.L, E), dtype=bool)
+        if w.n_resident >= 0:
+            for l in range(self.L):
+                self.resident[l] = synth.resident_mask(w, l).astype(bool)
+        table = np.where(self.resident, self.addr, np.uint64(0)).astype(np.uint64)
+        self.table_host = table.copy()
+        self.table = torch.from_numpy(table.view(np.int64)).to(self.device)
+        # upload: generate each layer into pinned staging, copy resident records to their slots
+        stage = torch.empty((E, rb), dtype=torch.uint8, pin_memory=True)
+        absent = [(l, e) for l in range(self.L) for e in range(E) if not self.resident[l, e]]
+        self.backing = torch.empty((max(1, len(absent)), rb), dtype=torch.uint8, pin_memory=True)
+        self.backing_index = {}
+        stream = torch.cuda.current_stream(self.device)
+        for l in range(self.L):
+            stream.synchronize()
+            synth.expert_records_into(stage.data_ptr(), w, l, 0, E, gen_threads)
+            self.routers[l].copy_(torch.from_numpy(synth.router(w, l)))
+            if self.bias is not None:
+                self.bias[l].copy_(torch.from_numpy(synth.zipf_bias(w, l)))
+            for e in range(E):
+                if self.resident[l, e]:
+                    p = int(self.pos[l, e])
+                    self.pool[p * rb:(p + 1) * rb].copy_(stage[e], non_blocking=True)
+                else:
+                    j = len(self.backing_index)
+                    self.backing[j].copy_(stage[e])
+                    self.backing_index[(l, e)] = j
+        stream.synchronize()
+        del stage
+
+    # -- helpers ------------------------------------------------------------------------
+    def expert_of_addr(self) -> dict:
+        """slot address -> (layer, expert), for checking slot tables."""
+        return {int(self.addr[l, e]): (l, e) for l in range(self.L) for e in range(self.w.n_experts)}
+
+    def record_host(self, layer: int, expert: int) -> np.ndarray:
+        import synth
+        return synth.expert_records(self.w, layer, expert, 1)[0]
+
+    def fill(self, layer: int, experts, stream=None) -> int:
+        """Copy the records of absent experts of `layer` from the pinned backing store into
+        their free slots and mark them resident (host table and device table row).
+        Returns the bytes copied."""
+        rb = self.record_bytes
+        s = stream or torch.cuda.current_stream(self.device)
+        n = 0
+        with torch.cuda.stream(s):
+            for e in experts:
+                if self.resident[layer, e]:
+                    continue
+                p = int(self.pos[layer, e])
+                self.pool[p * rb:(p + 1) * rb].copy_(self.backing[self.backing_index[(layer, e)]], non_blocking=True)
+                self.resident[layer, e] = True
+                self.table_host[layer, e] = self.addr[layer, e]
+                n += rb
+            row = torch.from_numpy(self.table_host[layer].view(np.int64).copy()).pin_memory()
+            self.table[layer].copy_(row, non_blocking=True)
+        return n
+
+    def reset_residency(self) -> None:
+        """Forget fills: mark the seeded absent experts absent again (their slots keep
+        whatever bytes they hold; the table no longer points at them)."""
+        import synth
+        if self.w.n_resident < 0:
+            return
+        for l in range(self.L):
+            self.resident[l] = synth.resident_mask(self.w, l).astype(bool)
+        self.table_host = np.where(self.resident, self.addr, np.uint64(0)).astype(np.uint64)
+        self.table.copy_(torch.from_numpy(self.table_host.view(np.int64).copy()))
+
+
+@dataclass
+class DecodeBuffers:
+    x: torch.Tensor          # [H] working residual stream of one token
+    xn: torch.Tensor         # [H]
+    ids: torch.Tensor        # [L][K] int32
+    weights: torch.Tensor    # [L][K] f32
+    slots: torch.Tensor      # [L][K] u64 (as int64)
+    logits: torch.Tensor     # [L][E] f32
+    miss: torch.Tensor       # [L] u32 (as int32)
+    ctrl: torch.Tensor       # [2] int32
+    route_ws: torch.Tensor
+    dec_ws: torch.Tensor
+
+    @staticmethod
+    def make(model: Model) -> "DecodeBuffers":
+        w, d = model.w, model.device
+        Lh, K, E, H = model.L, w.top_k, w.n_experts, w.hidden
+        shp = model.shape
+        return DecodeBuffers(
+            x=torch.zeros(H, dtype=torch.float32, device=d), xn=torch.zeros(H, dtype=torch.float32, device=d),
+            ids=torch.zeros((Lh, K), dtype=torch.int32, device=d),
+            weights=torch.zeros((Lh, K), dtype=torch.float32, device=d),
+            slots=torch.zeros((Lh, K), dtype=torch.int64, device=d),
+            logits=torch.zeros((Lh, E), dtype=torch.float32, device=d),
+            miss=torch.zeros(Lh, dtype=torch.int32, device=d),
+            ctrl=torch.tensor([RL_NO_EARLY_OUT, 0], dtype=torch.int32, device=d),
+            route_ws=torch.zeros(max(256, L.rl_route_workspace_bytes(shp, 1)), dtype=torch.uint8, device=d),
+            dec_ws=torch.empty(L.moe_decode_workspace_bytes(shp), dtype=torch.uint8, device=d))
+
+
+def enqueue_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
+                         stacked: bool, keep_logits: bool = False, x_hist: torch.Tensor | None = None) -> None:
+    """Enqueue one token through model.L layers on the current stream.
+
+    stacked=False (one layer, no norm, no residual): y_out = MoE(x_in).
+    stacked=True: x = x_in; per layer x = x + MoE(RMSNorm(x)) (the router and the experts
+    normalise x on the fly); y_out = x.
+    x_hist[l] (optional) receives layer l's input for per-layer checks."""
+    shp = model.shape
+    if not stacked:
+        for l in range(model.L):
+            L.rl_route(shp, l, 1, x_in, -1.0, model.routers[l], None if model.bias is None else model.bias[l],
+                       model.table, b.ids[l], b.weights[l], b.slots[l], b.miss, b.ctrl,
+                       b.logits[l] if keep_logits else None, b.route_ws, b.route_ws.numel())
+            L.moe_decode(shp, l, x_in, -1.0, b.slots[l], b.weights[l], model.codebook, y_out, 0, b.ctrl, b.dec_ws,
+                         b.dec_ws.numel())
+        return
+    b.x.copy_(x_in)
+    for l in range(model.L):
+        if x_hist is not None:
+            x_hist[l].copy_(b.x)
+        L.rl_route(shp, l, 1, b.x, EPS, model.routers[l], None if model.bias is None else model.bias[l],
+                   model.table, b.ids[l], b.weights[l], b.slots[l], b.miss, b.ctrl,
+                   b.logits[l] if keep_logits else None, b.route_ws, b.route_ws.numel())
+        L.moe_decode(shp, l, b.x, EPS, b.slots[l], b.weights[l], model.codebook, b.x, 1, b.ctrl, b.dec_ws,
+                     b.dec_ws.numel())
+    y_out.copy_(b.x)
+
+
+@dataclass
+class PrefillBuffers:
+    xn: torch.Tensor
+    ids: torch.Tensor
+    weights: torch.Tensor
+    slots: torch.Tensor
+    logits: torch.Tensor
+    miss: torch.Tensor
+    ctrl: torch.Tensor
+    offs: torch.Tensor
+    pair_tok: torch.Tensor
+    pair_k: torch.Tensor
+    route_ws: torch.Tensor
+    ws: torch.Tensor
+
+    @staticmethod
+    def make(model: Model, T: int) -> "PrefillBuffers":
+        w, d, shp = model.w, model.device, model.shape
+        K, E, H = w.top_k, w.n_experts, w.hidden
+        return PrefillBuffers(
+            xn=torch.zeros((T, H), dtype=torch.float32, device=d),
+            ids=torch.zeros((T, K), dtype=torch.int32, device=d),
+            weights=torch.zeros((T, K), dtype=torch.float32, device=d),
+            slots=torch.zeros((T, K), dtype=torch.int64, device=d),
+            logits=torch.zeros((T, E), dtype=torch.float32, device=d),
+            miss=torch.zeros(model.L, dtype=torch.int32, device=d),
+            ctrl=torch.tensor([RL_NO_EARLY_OUT, 0], dtype=torch.int32, device=d),
+            offs=torch.zeros(E + 1, dtype=torch.int32, device=d),
+            pair_tok=torch.zeros(max(1, T * K), dtype=torch.int32, device=d),
+            pair_k=torch.zeros(max(1, T * K), dtype=torch.uint8, device=d),
+            route_ws=torch.zeros(max(256, L.rl_route_workspace_bytes(shp, T)), dtype=torch.uint8, device=d),
+            ws=torch.empty(max(256, L.moe_prefill_workspace_bytes(shp, T)), dtype=torch.uint8, device=d))
+
+
+def _experts_fn(path: str):
+    return {"tc": L.moe_prefill_chunk, "f32": L.moe_prefill_chunk_f32}[path]
+
+
+def enqueue_prefill_route(model: Model, b: PrefillBuffers, layer: int, x: torch.Tensor, stacked: bool,
+                          keep_logits: bool = False) -> None:
+    T, shp = x.shape[0], model.shape
+    src = x
+    if stacked:
+        L.rl_rmsnorm(x, b.xn, T, model.w.hidden, EPS)
+        src = b.xn
+    L.rl_route(shp, layer, T, src, -1.0, model.routers[layer], None if model.bias is None else model.bias[layer],
+               model.table, b.ids, b.weights, b.slots, b.miss, b.ctrl, b.logits if keep_logits else None,
+               b.route_ws, b.route_ws.numel())
+
+
+def enqueue_prefill_experts(model: Model, b: PrefillBuffers, layer: int, x: torch.Tensor, y: torch.Tensor,
+                            stacked: bool, path: str = "tc") -> None:
+    T, shp = x.shape[0], model.shape
+    src = b.xn if stacked else x
+    L.rl_build_pairs(shp, layer, T, b.ids, b.offs, b.pair_tok, b.pair_k, b.ctrl)
+    _experts_fn(path)(shp, layer, T, src, b.offs, b.pair_tok, b.pair_k, b.slots, b.weights, model.codebook, y,
+                      1 if stacked else 0, b.ctrl, b.ws, b.ws.numel())
+
+
+@dataclass
+class BoundedStats:
+    miss: list
+    first_early_out: int
+    early_outs: list          # layers where the chain stopped
+    filled: list              # (layer, expert) in fill order
+    fill_bytes: int
+    fill_seconds: float
+    syncs: int
+
+
+def run_bounded_chunk(model: Model, b: PrefillBuffers, x: torch.Tensor, path: str = "tc", window: int | None = None,
+                      hist: dict | None = None) -> BoundedStats:
+    """Prefill chunk through model.L stacked layers with bounded residency.
+
+    The chain is enqueued `window` layers at a time (default: all remaining layers); the
+    host then reads the flag.  If a layer f stopped the chain, its distinct missing experts
+    are filled, its zero slots re-resolved, the flag reset, and the chain resumes with layer
+    f's experts.  x is updated in place (x <- x + MoE(RMSNorm(x)) per layer).
+    hist (optional): {"x": [L][T][H], "ids", "weights", "slots" ([L][T][K]), "logits" ([L][T][E])}
+    device tensors that receive each layer's input and its routing as rl_route wrote it
+    (slots before any fill)."""
+    hist = hist or {}
+    T, shp = x.shape[0], model.shape
+    Lh = model.L
+    window = Lh if window is None else window
+    stats = BoundedStats([0] * Lh, RL_NO_EARLY_OUT, [], [], 0, 0.0, 0)
+    b.miss.zero_()
+    b.ctrl[0] = RL_NO_EARLY_OUT
+    b.ctrl[1] = 0
+    layer = 0
+    resume_experts = False           # True: layer `layer` was routed already; run its experts
+    while layer < Lh:
+        end = min(Lh, layer + window)
+        for l in range(layer, end):
+            if not (resume_experts and l == layer):
+                if "x" in hist:
+                    hist["x"][l].copy_(x)
+                enqueue_prefill_route(model, b, l, x, True, keep_logits="logits" in hist)
+                for key, src in (("logits", b.logits), ("ids", b.ids), ("weights", b.weights), ("slots", b.slots)):
+                    if key in hist:
+                        hist[key][l].copy_(src)
+            enqueue_prefill_experts(model, b, l, x, x, True, path)
+        ctrl = b.ctrl.cpu()          # the host sync of the chain
+        stats.syncs += 1
+        if int(ctrl[1]) != 0:
+            raise RuntimeError(f"device error bits {int(ctrl[1])} at layer {layer}")
+        f = int(ctrl[0])
+        if f == RL_NO_EARLY_OUT:
+            layer = end
+            resume_experts = False
+            continue
+        # layer f selected absent experts: fill, re-resolve, reset the flag, resume at f's experts
+        t0 = time.perf_counter()
+        ids = b.ids.cpu().numpy()
+        slots = b.slots.cpu().numpy().view(np.uint64)
+        missing = sorted(set(int(e) for e in ids[slots == 0]))
+        nbytes = model.fill(f, missing)
+        L.rl_resolve_slots(shp, f, T, b.ids, model.table, b.slots)
+        b.ctrl[0] = RL_NO_EARLY_OUT
+        torch.cuda.current_stream().synchronize()
+        stats.fill_seconds += time.perf_counter() - t0
+        stats.fill_bytes += nbytes
+        stats.filled += [(f, e) for e in missing]
+        stats.early_outs.append(f)
+        if stats.first_early_out == RL_NO_EARLY_OUT:
+            stats.first_early_out = f
+        layer = f
+        resume_experts = True
+    stats.miss = [int(v) for v in b.miss.cpu().tolist()]
+    return stats

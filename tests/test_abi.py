@@ -1,0 +1,74 @@
+"""The C-ABI library: it loads, exports every symbol include/rl_moe.h declares, and answers
+the host-only queries (no kernel launch, no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_moe_expert_rl_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "rl_moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", src)) - {"sizeof"})
+
+
+def test_exports_every_declared_symbol(lib):
+    from quantized_moe_expert_rl_gb300 import _lib
+    declared = _declared()
+    assert set(declared) == set(_lib.EXPORTS), declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_host_queries(lib):
+    from quantized_moe_expert_rl_gb300._lib import RlShape
+    s = RlShape.of(2048, 512, 10, 512, 48)
+    assert lib.rl_abi_version() == 1
+    assert lib.rl_record_bytes(ctypes.byref(s)) == 811008
+    assert lib.moe_decode_workspace_bytes(ctypes.byref(s)) >= 10 * 512 * 4
+    assert lib.rl_route_workspace_bytes(ctypes.byref(s), 2048) >= 2048 * 512 * 4
+    assert lib.moe_prefill_workspace_bytes(ctypes.byref(s), 512) >= 5120 * 512 * 4 + 5120 * 2048 * 4
+    assert lib.rl_record_bytes(None) == 0
+
+
+def test_invalid_arguments_are_rejected_before_launch(lib):
+    """Checks that fail on the host: they return a status and launch nothing, so they run
+    without a GPU."""
+    from quantized_moe_expert_rl_gb300._lib import RL_ERR_INVALID, RL_ERR_UNSUPPORTED, RlShape
+    good = RlShape.of(2048, 512, 10, 512, 48)
+    fake = ctypes.c_void_p(1 << 20)
+    # layer out of range
+    st = lib.rl_route(ctypes.byref(good), 48, 1, fake, -1.0, fake, None, fake, fake, fake, fake, fake, fake, fake, None,
+                      0, None)
+    assert st == RL_ERR_INVALID and b"layer" in lib.rl_last_error()
+    # NULL required buffer
+    st = lib.moe_decode(ctypes.byref(good), 0, None, -1.0, fake, fake, fake, fake, 0, fake, fake, 1 << 20, None)
+    assert st == RL_ERR_INVALID
+    # workspace too small
+    st = lib.moe_decode(ctypes.byref(good), 0, fake, -1.0, fake, fake, fake, fake, 0, fake, fake, 16, None)
+    assert st == RL_ERR_INVALID and b"workspace" in lib.rl_last_error()
+    # unsupported shapes
+    for bad in (RlShape.of(384, 512, 10, 512, 1), RlShape.of(2048, 1024, 10, 512, 1),
+                RlShape.of(2048, 512, 17, 512, 1), RlShape.of(2048, 512, 10, 200, 1)):
+        st = lib.rl_build_pairs(ctypes.byref(bad), 0, 4, fake, fake, fake, fake, fake, None, 0, None)
+        assert st == RL_ERR_UNSUPPORTED, bad
+    # top_k > n_experts
+    st = lib.rl_build_pairs(ctypes.byref(RlShape.of(512, 8, 10, 128, 1)), 0, 4, fake, fake, fake, fake, fake, None,
+                            0, None)
+    assert st == RL_ERR_INVALID
+    # prefill workspace too small / misaligned
+    st = lib.moe_prefill_chunk(ctypes.byref(good), 0, 512, fake, fake, fake, fake, fake, fake, fake, fake, 0, fake,
+                               fake, 1024, None)
+    assert st == RL_ERR_INVALID
+    st = lib.rl_rmsnorm(fake, fake, 4, 2048, -1.0, None)
+    assert st == RL_ERR_INVALID

@@ -1,0 +1,138 @@
+"""Prefill parity on the GPU: the 512-token chunk (routing of every token, the expert-sorted
+pair list bit-exact, outputs of sampled tokens), and the 48-layer, 2048-token chunk with Zipf
+router bias and 85% residency (exact per-layer miss counts, first early-out layer, fills,
+routing of every token in every layer, outputs of sampled tokens in sampled layers)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from tests._gpu_common import REL_BF16, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
+
+PATHS = [("f32", REL_F32), ("tc", REL_BF16)]
+
+
+def _engine():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from quantized_moe_expert_rl_gb300 import engine
+    return engine
+
+
+@pytest.fixture(scope="module")
+def chunk_model():
+    engine = _engine()
+    w = synth.WORKLOADS["prefill_chunk"]
+    m = engine.Model(w)
+    return w, m, OracleSide(m)
+
+
+@pytest.mark.parametrize("path,tol", PATHS)
+def test_prefill_chunk(chunk_model, path, tol):
+    engine = _engine()
+    w, m, o = chunk_model
+    T = w.tokens
+    b = engine.PrefillBuffers.make(m, T)
+    x = torch.from_numpy(synth.tokens(w)).cuda()
+    y = torch.zeros_like(x)
+    engine.enqueue_prefill_route(m, b, 0, x, stacked=False, keep_logits=True)
+    engine.enqueue_prefill_experts(m, b, 0, x, y, stacked=False, path=path)
+    torch.cuda.synchronize()
+    assert b.ctrl.tolist() == [0x7FFFFFFF, 0]
+    xo = x.double().cpu().numpy()
+    rep = {}
+    r = check_route(b.logits.cpu().numpy(), b.ids.cpu().numpy(), b.weights.cpu().numpy(), u64(b.slots),
+                    oracle.router_logits(xo, o.router(0)), o.table_row(0), w.top_k, 0, rep)
+    offs, ptok, pk = oracle.build_pairs(r.ids, w.n_experts)
+    P = T * w.top_k
+    assert np.array_equal(b.offs.cpu().numpy().astype(np.uint32), offs)
+    assert np.array_equal(b.pair_tok[:P].cpu().numpy().astype(np.uint32), ptok)
+    assert np.array_equal(b.pair_k[:P].cpu().numpy(), pk)
+    sample = np.arange(0, T, 16)
+    y_o = o.experts(xo[sample], r.ids[sample], r.weights[sample], r.slots[sample])
+    err = rel_l2(y.cpu().numpy()[sample], y_o)
+    print(f"prefill_chunk {path}: rel L2 {err:.2e} over {len(sample)} tokens, near ties {rep.get('near_ties', 0)}")
+    assert err <= tol
+
+
+def test_prefill_paths_agree(chunk_model):
+    """The two grouped paths on the same routing: bf16 tensor-core result within the bf16
+    bound of the f32 CUDA-core result over every token."""
+    engine = _engine()
+    w, m, _ = chunk_model
+    b = engine.PrefillBuffers.make(m, w.tokens)
+    x = torch.from_numpy(synth.tokens(w)).cuda()
+    ys = {}
+    engine.enqueue_prefill_route(m, b, 0, x, stacked=False)
+    for path in ("f32", "tc"):
+        y = torch.zeros_like(x)
+        engine.enqueue_prefill_experts(m, b, 0, x, y, stacked=False, path=path)
+        torch.cuda.synchronize()
+        ys[path] = y.double().cpu().numpy()
+    assert rel_l2(ys["tc"], ys["f32"]) <= REL_BF16
+
+
+@pytest.fixture(scope="module")
+def bounded_model():
+    engine = _engine()
+    w = synth.WORKLOADS["prefill_bounded"]
+    m = engine.Model(w)
+    return w, m, OracleSide(m)
+
+
+@pytest.mark.parametrize("path,tol", PATHS)
+def test_prefill_bounded(bounded_model, path, tol):
+    engine = _engine()
+    w, m, o = bounded_model
+    m.reset_residency()
+    T, Lh = w.tokens, m.L
+    b = engine.PrefillBuffers.make(m, T)
+    x = torch.from_numpy(synth.tokens(w)).cuda()
+    K = w.top_k
+    hist = {"x": torch.zeros((Lh + 1, T, w.hidden), dtype=torch.float32, device="cuda"),
+            "ids": torch.zeros((Lh, T, K), dtype=torch.int32, device="cuda"),
+            "weights": torch.zeros((Lh, T, K), dtype=torch.float32, device="cuda"),
+            "slots": torch.zeros((Lh, T, K), dtype=torch.int64, device="cuda"),
+            "logits": torch.zeros((Lh, T, w.n_experts), dtype=torch.float32, device="cuda")}
+    table0 = m.table_host.copy()
+    st = engine.run_bounded_chunk(m, b, x, path=path, hist=hist)
+    hist["x"][Lh].copy_(x)
+    torch.cuda.synchronize()
+    assert b.ctrl.tolist() == [0x7FFFFFFF, 0]
+    # exact per-layer miss counts and fills from the GPU's selections against the seeded table
+    ids_all = hist["ids"].cpu().numpy()
+    lg_all = hist["logits"].cpu().numpy()
+    w_all = hist["weights"].cpu().numpy()
+    s_all = u64(hist["slots"])
+    first = 0x7FFFFFFF
+    for l in range(Lh):
+        r = oracle.route_from_logits(lg_all[l], table0[l], w.top_k, l)
+        assert np.array_equal(r.ids, ids_all[l]), l
+        assert st.miss[l] == r.miss, (l, st.miss[l], r.miss)
+        if r.miss and first == 0x7FFFFFFF:
+            first = l
+        missing = sorted(set(int(e) for e in r.ids[r.slots == 0]))
+        assert [e for (lf, e) in st.filled if lf == l] == missing
+    assert st.first_early_out == first
+    assert st.early_outs == [l for l in range(Lh) if st.miss[l] > 0]
+    print(f"bounded {path}: misses per layer {st.miss}; first early-out {first}; "
+          f"{len(st.filled)} experts filled ({st.fill_bytes / 2**20:.0f} MiB)")
+    # routing accuracy of every token in every layer, outputs of sampled tokens in sampled layers
+    X = hist["x"].cpu().numpy().astype(np.float64)
+    rep, worst = {}, 0.0
+    sample_t = np.arange(5, T, 256)
+    for l in range(Lh):
+        xn = oracle.rmsnorm(X[l])
+        lg64 = oracle.router_logits(xn, o.router(l), o.bias(l))
+        slots_l = m.table_host[l][ids_all[l].astype(np.int64)]
+        r = check_route(lg_all[l], ids_all[l], w_all[l], s_all[l], lg64, table0[l], w.top_k, l, rep)
+        if l % 8 == 3:
+            y_o = oracle.moe_experts(xn[sample_t], r.ids[sample_t], r.weights[sample_t], slots_l[sample_t],
+                                     o.record, w.hidden, w.inter, o.grid)
+            err = rel_l2(X[l + 1][sample_t] - X[l][sample_t], y_o)
+            worst = max(worst, err)
+            assert err <= tol, (l, err)
+    print(f"bounded {path}: worst sampled-layer rel L2 {worst:.2e}; near ties {rep.get('near_ties', 0)}")

@@ -151,6 +151,28 @@ rl_status moe_decode(const rl_moe_shape *shp, int32_t layer, const float *x, flo
                      int32_t *ctrl, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_decode_static - moe_decode with no workspace argument, for callers that cannot
+ * allocate device memory: for instance a plugin or extension hosted by another program that
+ * owns every device allocation and only passes in the tensors of the call, or a serving loop
+ * that forbids allocation after start-up.  The K * inter floats of h scratch that moe_decode
+ * takes from `ws` come instead from a fixed array inside the library
+ * (RL_STATIC_SCRATCH_FLOATS floats = 64 KB, held on every device that loads the library until
+ * the process exits).  The arguments and results are those of moe_decode.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - Every call on a device shares the one array: calls that overlap on the GPU (other
+ *     streams, other host threads) race; serialise them.
+ *   - top_k * inter above RL_STATIC_SCRATCH_FLOATS returns RL_ERR_UNSUPPORTED (with the
+ *     supported shapes it always fits).
+ * The Red Lite pages have no counterpart of this entry point.
+ */
+#define RL_STATIC_SCRATCH_FLOATS 16384
+rl_status moe_decode_static(const rl_moe_shape *shp, int32_t layer, const float *x, float norm_eps,
+                            const uint64_t *slots, const float *weights, const int8_t *codebook, float *y,
+                            int32_t accumulate, int32_t *ctrl, void *stream);
+
+/*
  * rl_build_pairs - (expert, token) pairs sorted by expert, stable in (t, k) order
  * ("Red Lite dev20", "What changed", item 3):
  *   offs[e] .. offs[e+1]-1 index the pairs of expert e; pair p is (pair_tok[p], pair_k[p]).

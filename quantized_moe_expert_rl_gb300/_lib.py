@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "RL_OK", 1: "RL_ERR_INVALID", 2: "RL_ERR_UNSUPPORTED", 3: "RL
 EXPORTS = ("rl_abi_version", "rl_last_error", "rl_record_bytes", "rl_rmsnorm", "rl_route_workspace_bytes",
            "rl_route", "rl_resolve_slots", "moe_decode_workspace_bytes", "moe_decode",
            "rl_build_pairs_workspace_bytes", "rl_build_pairs", "moe_prefill_workspace_bytes",
-           "moe_prefill_chunk", "moe_prefill_chunk_f32")
+           "moe_prefill_chunk", "moe_prefill_chunk_f32", "moe_decode_static")
 
 
 class RlShape(ctypes.Structure):
@@ -63,6 +63,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "rl_resolve_slots": (i32, [shp, i32, i32, vp, vp, vp, vp]),
         "moe_decode_workspace_bytes": (sz, [shp]),
         "moe_decode": (i32, [shp, i32, vp, f32, vp, vp, vp, vp, i32, vp, vp, sz, vp]),
+        "moe_decode_static": (i32, [shp, i32, vp, f32, vp, vp, vp, vp, i32, vp, vp]),
         "rl_build_pairs_workspace_bytes": (sz, [shp, i32]),
         "rl_build_pairs": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_prefill_workspace_bytes": (sz, [shp, i32]),
@@ -137,6 +138,12 @@ def moe_decode(shape, layer, x, norm_eps, slots, weights, codebook, y, accumulat
     _check("moe_decode", load().moe_decode(ctypes.byref(shape), layer, ptr(x), float(norm_eps), ptr(slots), ptr(weights),
                                            ptr(codebook), ptr(y), int(accumulate), ptr(ctrl), ptr(ws), ws_bytes,
                                            _stream(stream)))
+
+
+def moe_decode_static(shape, layer, x, norm_eps, slots, weights, codebook, y, accumulate, ctrl, stream=None):
+    _check("moe_decode_static", load().moe_decode_static(ctypes.byref(shape), layer, ptr(x), float(norm_eps),
+                                                         ptr(slots), ptr(weights), ptr(codebook), ptr(y),
+                                                         int(accumulate), ptr(ctrl), _stream(stream)))
 
 
 def rl_build_pairs_workspace_bytes(shape, T) -> int:

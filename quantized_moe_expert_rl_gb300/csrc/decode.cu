@@ -18,6 +18,7 @@
 // after it.  With norm_eps >= 0 the input is the raw residual x and is RMS-normalised on the
 // fly with the same deterministic scale rl_rmsnorm computes.
 #include <algorithm>
+#include <mutex>
 
 #include "qdot.cuh"
 
@@ -320,4 +321,52 @@ extern "C" rl_status moe_decode(const rl_moe_shape *shp, int32_t layer, const fl
         case 1024: return launch_down<4, 32>(slots, weights, codebook, h, y, accumulate, ctrl, layer, H, I, K, s);
         default: return launch_down<8, 32>(slots, weights, codebook, h, y, accumulate, ctrl, layer, H, I, K, s);
     }
+}
+
+// ---------------------------------------------------------------------------------------------
+// moe_decode_static: moe_decode for callers that cannot hand the library any device memory
+// of its own (see rl_moe.h).  The h scratch lives in this fixed device array instead of a
+// caller workspace.  The array exists once per device that loads the library, for the life of
+// the process; every call on a device shares it, so calls that overlap on the GPU race.  Each
+// call overwrites every h entry it later reads, so nothing needs clearing between calls.
+// ---------------------------------------------------------------------------------------------
+static __device__ __align__(256) float g_static_h[RL_STATIC_SCRATCH_FLOATS];
+
+namespace rl {
+// Device address of g_static_h on the current device.  In host code the array's name is
+// only a host-side stand-in, so the address is asked of the runtime once per device (with
+// that device current) and cached.
+static rl_status static_scratch(float **out) {
+    static std::mutex mu;
+    static float *addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(RL_ERR_CUDA, "moe_decode_static: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(RL_ERR_UNSUPPORTED, "moe_decode_static: device %d", dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_h);
+        if (e != cudaSuccess || !p)
+            return fail(RL_ERR_CUDA, "moe_decode_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        addr[dev] = static_cast<float *>(p);
+    }
+    *out = addr[dev];
+    return RL_OK;
+}
+}  // namespace rl
+
+extern "C" rl_status moe_decode_static(const rl_moe_shape *shp, int32_t layer, const float *x, float norm_eps,
+                                       const uint64_t *slots, const float *weights, const int8_t *codebook, float *y,
+                                       int32_t accumulate, int32_t *ctrl, void *stream) {
+    rl_status st = check_shape(shp);
+    if (st != RL_OK) return st;
+    if ((size_t)shp->top_k * shp->inter > RL_STATIC_SCRATCH_FLOATS)
+        return fail(RL_ERR_UNSUPPORTED, "moe_decode_static: top_k * inter = %d exceeds the fixed scratch of %d floats",
+                    shp->top_k * shp->inter, RL_STATIC_SCRATCH_FLOATS);
+    float *h = nullptr;
+    st = static_scratch(&h);
+    if (st != RL_OK) return st;
+    return moe_decode(shp, layer, x, norm_eps, slots, weights, codebook, y, accumulate, ctrl, h,
+                      (size_t)RL_STATIC_SCRATCH_FLOATS * sizeof(float), stream);
 }

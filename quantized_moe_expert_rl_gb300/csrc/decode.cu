@@ -24,79 +24,180 @@
 
 namespace rl {
 
-constexpr int kGuThreads = 512;
+constexpr int kGuThreads = 1024;
 constexpr int kDnRows = 16;
 
 // rows of the flat (expert, row) space handled together so that copies stay 16-byte multiples
 __host__ __device__ inline int gu_unit(int H) { return H >= 2048 ? 1 : 2048 / H; }
+// warps per row: wide rows are split in two halves so that a lane holds only 32 inputs
+__host__ __device__ inline int gu_split(int H) { return H >= 1024 ? 2 : 1; }
+
+constexpr int kGuChunks = 4;  // row chunks per expert segment, each with its own mbarrier
 
 struct GuLayout {
     int rowb, rmax;  // bytes of one H-wide row; max rows per CTA
-    size_t total;
+    size_t tiles, part, total;
     __host__ __device__ GuLayout(int H, int I, int K, int G) {
         rowb = (int)matrix_bytes(1, H);
         const int U = gu_unit(H), units = K * I / U;
         rmax = ((units + G - 1) / G) * U;
         // gate and up rows of <= rmax pairs; >= 2 KB because it first stages the codebook
-        total = 128 + kTabBytes + std::max((size_t)2048, 2 * (size_t)rmax * rowb);
+        tiles = std::max((size_t)2048, 2 * (size_t)rmax * rowb);
+        part = align_up((size_t)rmax * 4 * sizeof(float), 16);  // [row][half][gate, up]
+        total = 128 + kTabBytes + (size_t)H * sizeof(float) + part + tiles;
     }
 };
 
-template <int GPL, bool NORM>
+// Partial (gate, up) dots of one lane for one row pair.
+template <int GPL>
+__device__ __forceinline__ void gu_row(const uint8_t *gb, const uint8_t *ub, int g0, const float *xv,
+                                       const uint4 *tabc, float &gv, float &uv) {
+    float ge = 0.f, go = 0.f, ue = 0.f, uo = 0.f;
+#pragma unroll
+    for (int g = 0; g < GPL; ++g) {
+        group_fma_s(*reinterpret_cast<const uint16_t *>(gb + 2 + 2 * (g0 + g)), &xv[8 * g], tabc, ge, go);
+        group_fma_s(*reinterpret_cast<const uint16_t *>(ub + 2 + 2 * (g0 + g)), &xv[8 * g], tabc, ue, uo);
+    }
+    gv = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(gb)) * (ge + go);
+    uv = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(ub)) * (ue + uo);
+}
+
+// GPL = groups (8 values) per lane = H / (256 * SPLIT); SPLIT warps per (gate, up) row pair.
+template <int GPL, int SPLIT, bool NORM>
 __global__ void __launch_bounds__(kGuThreads) dec_gateup_kernel(const float *__restrict__ xin, float eps,
                                                                 const uint64_t *__restrict__ slots,
                                                                 const int8_t *__restrict__ codebook,
                                                                 float *__restrict__ h, int32_t *ctrl, int layer,
                                                                 int H, int I, int K) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // [2]
-    float *scale_s = reinterpret_cast<float *>(smem + 16);
-    int *ok_s = reinterpret_cast<int *>(smem + 20);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // [2 segments][kGuChunks]
+    float *scale_s = reinterpret_cast<float *>(smem + 8 * 2 * kGuChunks);
+    int *ok_s = reinterpret_cast<int *>(smem + 8 * 2 * kGuChunks + 4);
     uint4 *tab = reinterpret_cast<uint4 *>(smem + 128);
+    const GuLayout lay(H, I, K, gridDim.x);
+    float *x_s = reinterpret_cast<float *>(smem + 128 + kTabBytes);
+    float *part = x_s + H;
     // [seg 0 gate | seg 0 up | seg 1 gate | seg 1 up], n0 and n1 rows; every row count is a
     // multiple of gu_unit(H), so every sub-tile starts 16-byte aligned
-    uint8_t *tiles = smem + 128 + kTabBytes;
-    const GuLayout lay(H, I, K, gridDim.x);
+    uint8_t *tiles = reinterpret_cast<uint8_t *>(part) + lay.part;
     const int U = gu_unit(H), units = K * I / U;
     const int p0 = (int)((long long)blockIdx.x * units / gridDim.x) * U;
     const int p1 = (int)((long long)(blockIdx.x + 1) * units / gridDim.x) * U;
     const int ka = p0 / I, kb = (p1 - 1) / I;  // at most two experts (p1 - p0 <= I)
     const int n0 = (ka == kb ? p1 : (ka + 1) * I) - p0, n1 = (p1 - p0) - n0;
+    // chunk c of segment s holds rows [cut(s, c), cut(s, c + 1)) of the segment
+    auto cut = [&](int seg, int c) { return ((seg == 0 ? n0 : n1) / U * c / kGuChunks) * U; };
     if (threadIdx.x == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < 2 * kGuChunks; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
     }
-    build_pair_table(tab, codebook, reinterpret_cast<uint2 *>(tiles));  // tiles are free until the copies
+    build_pair_table(tab, codebook, nullptr);  // ends with __syncthreads
     pdl_wait();
-    if (ld_ctrl(ctrl) <= layer) return;
-    if (threadIdx.x == 0) {
-        const uint64_t sa = slots[ka], sb = slots[kb];
-        int ok = 1;
-        if (sa == 0 || (sa & 15)) { dev_error(ctrl, sa == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN); ok = 0; }
-        if (sb == 0 || (sb & 15)) { dev_error(ctrl, sb == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN); ok = 0; }
-        *ok_s = ok;
+    // independent loads first: the flag, the two slots, x
+    const int flag = ld_ctrl(ctrl);
+    uint64_t sa = 0, sb = 0;
+    if (threadIdx.x < 32) {
+        sa = __ldcg(slots + ka);
+        sb = __ldcg(slots + kb);
+    }
+    for (int i = threadIdx.x; i < H / 4; i += blockDim.x)
+        reinterpret_cast<float4 *>(x_s)[i] = __ldcg(reinterpret_cast<const float4 *>(xin) + i);
+    if (flag <= layer) return;
+    if (threadIdx.x < 32) {
+        const bool ok = sa != 0 && (sa & 15) == 0 && sb != 0 && (sb & 15) == 0;
+        if (threadIdx.x == 0) {
+            if (sa == 0 || (sa & 15)) dev_error(ctrl, sa == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN);
+            if (sb == 0 || (sb & 15)) dev_error(ctrl, sb == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN);
+            *ok_s = ok;
+        }
         if (ok) {
-            const size_t matb = matrix_bytes(I, H);
-            const int ia = p0 - ka * I;
-            const uint32_t b0 = (uint32_t)(n0 * lay.rowb);
-            mbar_arrive_expect_tx(&bars[0], 2 * b0);
-            const uint8_t *A = reinterpret_cast<const uint8_t *>(sa);
-            bulk_g2s(tiles, A + (size_t)ia * lay.rowb, b0, &bars[0]);
-            bulk_g2s(tiles + b0, A + matb + (size_t)ia * lay.rowb, b0, &bars[0]);
-            if (n1 > 0) {
-                const uint32_t b1 = (uint32_t)(n1 * lay.rowb);
-                mbar_arrive_expect_tx(&bars[1], 2 * b1);
-                const uint8_t *B = reinterpret_cast<const uint8_t *>(sb);
-                bulk_g2s(tiles + 2 * b0, B, b1, &bars[1]);
-                bulk_g2s(tiles + 2 * b0 + b1, B + matb, b1, &bars[1]);
+            // lane i < 2 * kGuChunks issues chunk (seg = i / kGuChunks, c = i % kGuChunks):
+            // its gate rows and its up rows, completion on bars[i]
+            const int seg = threadIdx.x / kGuChunks, c = threadIdx.x % kGuChunks;
+            if (threadIdx.x < 2 * kGuChunks) {
+                const int n = seg == 0 ? n0 : n1;
+                const int r0 = cut(seg, c), r1 = cut(seg, c + 1);
+                if (r1 > r0) {
+                    const size_t matb = matrix_bytes(I, H);
+                    const uint8_t *base = reinterpret_cast<const uint8_t *>(seg == 0 ? sa : sb);
+                    const int ia = seg == 0 ? p0 - ka * I : 0;  // first row of the segment in the expert
+                    const uint32_t bytes = (uint32_t)((r1 - r0) * lay.rowb);
+                    uint8_t *gdst = tiles + (seg == 0 ? 0 : 2 * (size_t)n0 * lay.rowb) + (size_t)r0 * lay.rowb;
+                    mbar_arrive_expect_tx(&bars[threadIdx.x], 2 * bytes);
+                    bulk_g2s(gdst, base + (size_t)(ia + r0) * lay.rowb, bytes, &bars[threadIdx.x]);
+                    bulk_g2s(gdst + (size_t)n * lay.rowb, base + matb + (size_t)(ia + r0) * lay.rowb, bytes,
+                             &bars[threadIdx.x]);
+                }
             }
         }
     }
-    // Warm L2 with the down matrices the next kernel reads: CTA c prefetches the c-th slice of
-    // every selected expert's down matrix (slots are final once this kernel runs).
-    if (threadIdx.x >= 32 && threadIdx.x < 32 + K) {
-        const uint64_t sd = slots[threadIdx.x - 32];
+    __syncthreads();  // x staged, ok_s written
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (NORM && warp == 0) {
+        const float r = rms_scale_warp(x_s, H, eps);
+        if (lane == 0) *scale_s = r;
+    }
+    __syncthreads();
+    if (!*ok_s) return;
+    pdl_trigger();
+    const int half = warp % SPLIT, team = warp / SPLIT;
+    constexpr int kTeams = kGuThreads / 32 / SPLIT;
+    // lane's 8*GPL consecutive inputs: columns half*H/SPLIT + lane*8*GPL ...
+    const int c0 = half * (H / SPLIT) + lane * 8 * GPL;
+    float xv[8 * GPL];
+    {
+        const float r = NORM ? *scale_s : 1.f;
+#pragma unroll
+        for (int q = 0; q < 2 * GPL; ++q) {
+            const float4 v = reinterpret_cast<const float4 *>(x_s + c0)[q];
+            xv[4 * q] = v.x * r; xv[4 * q + 1] = v.y * r; xv[4 * q + 2] = v.z * r; xv[4 * q + 3] = v.w * r;
+        }
+    }
+    const uint4 *tabc = tab + (lane & (kTabCopies - 1));
+    const int gl = c0 / 8, boff = (gl >> 5) * kBlockBytes, g0 = gl & 31;  // lane's groups inside the row
+    unsigned ready = 0;  // bit i: bars[i] observed complete by this warp
+    bool timed_out = false;
+    auto locate = [&](int p, const uint8_t *&gb, const uint8_t *&ub) {
+        const int seg = p - p0 < n0 ? 0 : 1;
+        const int r = seg == 0 ? p - p0 : p - p0 - n0;
+        const int n = seg == 0 ? n0 : n1;
+        int c = 0;
+        while (c + 1 < kGuChunks && r >= cut(seg, c + 1)) ++c;
+        const int bi = seg * kGuChunks + c;
+        if (!(ready & (1u << bi))) {
+            if (!mbar_wait(&bars[bi], 0)) timed_out = true;
+            ready |= 1u << bi;
+        }
+        gb = tiles + (seg == 0 ? 0 : 2 * (size_t)n0 * lay.rowb) + (size_t)r * lay.rowb + boff;
+        ub = gb + (size_t)n * lay.rowb;
+    };
+    for (int p = p0 + team; p < p1; p += 2 * kTeams) {
+        const int q = p + kTeams;  // second row pair in flight
+        const uint8_t *gb, *ub, *gb2 = nullptr, *ub2 = nullptr;
+        locate(p, gb, ub);
+        if (q < p1) locate(q, gb2, ub2);
+        if (timed_out) break;
+        float gv, uv, gv2 = 0.f, uv2 = 0.f;
+        gu_row<GPL>(gb, ub, g0, xv, tabc, gv, uv);
+        if (q < p1) gu_row<GPL>(gb2, ub2, g0, xv, tabc, gv2, uv2);
+        gv = warp_sum(gv);
+        uv = warp_sum(uv);
+        gv2 = warp_sum(gv2);
+        uv2 = warp_sum(uv2);
+        if (lane == 0) {
+            part[((p - p0) * 2 + half) * 2 + 0] = gv;
+            part[((p - p0) * 2 + half) * 2 + 1] = uv;
+            if (q < p1) {
+                part[((q - p0) * 2 + half) * 2 + 0] = gv2;
+                part[((q - p0) * 2 + half) * 2 + 1] = uv2;
+            }
+        }
+    }
+    if (timed_out && lane == 0) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
+    // Warm L2 with the down matrices the next kernel reads (CTA c takes the c-th slice of every
+    // selected expert's down matrix); issued after this CTA's own rows are in shared memory.
+    if (warp == 0 && lane < K && !timed_out) {
+        const uint64_t sd = __ldcg(slots + lane);
         if (sd != 0 && (sd & 15) == 0) {
             const size_t matb = matrix_bytes(I, H);
             const size_t per = align_up((matb + gridDim.x - 1) / gridDim.x, 256);
@@ -106,63 +207,12 @@ __global__ void __launch_bounds__(kGuThreads) dec_gateup_kernel(const float *__r
                                  (uint32_t)std::min(per, matb - off));
         }
     }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // lane's 8*GPL consecutive inputs as packed pairs
-    unsigned long long xp[4 * GPL];
-#pragma unroll
-    for (int q = 0; q < 2 * GPL; ++q) {
-        const float4 v = reinterpret_cast<const float4 *>(xin + lane * 8 * GPL)[q];
-        xp[2 * q] = pack2(__float_as_uint(v.x), __float_as_uint(v.y));
-        xp[2 * q + 1] = pack2(__float_as_uint(v.z), __float_as_uint(v.w));
-    }
-    if (NORM && warp == 0) {
-        const float r = rms_scale_warp(xin, H, eps);
-        if (lane == 0) *scale_s = r;
-    }
     __syncthreads();
-    if (!*ok_s) return;
-    pdl_trigger();
-    if (NORM) {
-        const float r = *scale_s;
-#pragma unroll
-        for (int q = 0; q < 4 * GPL; ++q)
-            xp[q] = pack2(__float_as_uint(__uint_as_float((uint32_t)xp[q]) * r),
-                          __float_as_uint(__uint_as_float((uint32_t)(xp[q] >> 32)) * r));
-    }
-    const uint4 *tabc = tab + (lane & (kTabCopies - 1));
-    const int gl = lane * GPL, boff = (gl >> 5) * kBlockBytes, g0 = gl & 31;
-    bool ready0 = false, ready1 = false;
-    for (int p = p0 + warp; p < p1; p += kGuThreads / 32) {
-        const int seg = p - p0 < n0 ? 0 : 1;
-        bool &ready = seg == 0 ? ready0 : ready1;
-        if (!ready) {
-            if (!mbar_wait(&bars[seg], 0)) {
-                if (lane == 0) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
-                return;
-            }
-            ready = true;
-        }
-        const int r = seg == 0 ? p - p0 : p - p0 - n0;
-        const size_t nseg = seg == 0 ? n0 : n1;  // rows in this segment
-        const uint8_t *gb = tiles + (seg == 0 ? 0 : 2 * (size_t)n0 * lay.rowb) + (size_t)r * lay.rowb + boff;
-        const uint8_t *ub = gb + nseg * lay.rowb;
-        unsigned long long ag0 = 0, ag1 = 0, au0 = 0, au1 = 0;
-#pragma unroll
-        for (int g = 0; g < GPL; g += 2) {
-            ag0 = group_fma(*reinterpret_cast<const uint16_t *>(gb + 2 + 2 * (g0 + g)), &xp[4 * g], tabc, ag0);
-            au0 = group_fma(*reinterpret_cast<const uint16_t *>(ub + 2 + 2 * (g0 + g)), &xp[4 * g], tabc, au0);
-            if (g + 1 < GPL) {
-                ag1 = group_fma(*reinterpret_cast<const uint16_t *>(gb + 4 + 2 * (g0 + g)), &xp[4 * (g + 1)], tabc,
-                                ag1);
-                au1 = group_fma(*reinterpret_cast<const uint16_t *>(ub + 4 + 2 * (g0 + g)), &xp[4 * (g + 1)], tabc,
-                                au1);
-            }
-        }
-        const float dg = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(gb));
-        const float du = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(ub));
-        const float gv = warp_sum(dg * (hsum2(ag0) + hsum2(ag1)));
-        const float uv = warp_sum(du * (hsum2(au0) + hsum2(au1)));
-        if (lane == 0) h[p] = silu(gv) * uv;  // p = k * I + i
+    if (timed_out) return;
+    for (int t = threadIdx.x; t < p1 - p0; t += blockDim.x) {
+        float gv = part[t * 4 + 0], uv = part[t * 4 + 1];
+        if (SPLIT == 2) { gv += part[t * 4 + 2]; uv += part[t * 4 + 3]; }
+        h[p0 + t] = silu(gv) * uv;  // p = k * I + i
     }
 }
 
@@ -175,7 +225,8 @@ struct DnLayout {
     }
 };
 
-// Rows of I values: LPR lanes per row (min(32, I/8)), GPL groups per lane; one warp per expert.
+// Rows of I values: LPR lanes per row (min(32, I/8)), GPL groups per lane; two warps per
+// expert, 8 rows each.
 template <int GPL, int LPR>
 __global__ void dec_down_kernel(const uint64_t *__restrict__ slots, const float *__restrict__ weights,
                                 const int8_t *__restrict__ codebook, const float *__restrict__ h,
@@ -183,7 +234,6 @@ __global__ void dec_down_kernel(const uint64_t *__restrict__ slots, const float 
                                 int K) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
-    int *ok_s = reinterpret_cast<int *>(smem + 16);
     uint4 *tab = reinterpret_cast<uint4 *>(smem + 128);
     const DnLayout lay(I, K);
     uint8_t *tiles = smem + 128 + kTabBytes;
@@ -193,36 +243,35 @@ __global__ void dec_down_kernel(const uint64_t *__restrict__ slots, const float 
         mbar_init(bar, 1);
         fence_mbar_init();
     }
-    build_pair_table(tab, codebook, reinterpret_cast<uint2 *>(tiles));  // tiles are free until the copies
+    build_pair_table(tab, codebook, nullptr);
     pdl_wait();
-    if (ld_ctrl(ctrl) <= layer) return;
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        for (int k = 0; k < K; ++k) {
-            const uint64_t s = slots[k];
-            if (s == 0 || (s & 15)) { dev_error(ctrl, s == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN); ok = 0; }
-        }
-        *ok_s = ok;
-        if (ok) {
-            // kDnRows rows of I values start on a block boundary (kDnRows * I % 2048 == 0)
-            const uint32_t bytes = (uint32_t)matrix_bytes(kDnRows, I);
-            const size_t off = 2 * matrix_bytes(I, H) + matrix_bytes(r0, I);
-            mbar_arrive_expect_tx(bar, bytes * K);
-            for (int k = 0; k < K; ++k)
-                bulk_g2s(tiles + k * lay.tileb, reinterpret_cast<const uint8_t *>(slots[k]) + off, bytes, bar);
-        }
-    }
-    __syncthreads();
-    if (!*ok_s) return;
-    const int lane = threadIdx.x & 31, k = threadIdx.x >> 5;  // one warp per expert
+    // independent loads first: the flag, the K slots, this warp's slice of h
+    const int flag = ld_ctrl(ctrl);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int k = warp >> 1, r_lo = (warp & 1) * (kDnRows / 2);  // two warps per expert
     const int sub = lane / LPR, sl = lane % LPR;
     constexpr int kRowsPerPass = 32 / LPR;
-    unsigned long long hp[4 * GPL];
+    uint64_t sk = 0;
+    if (threadIdx.x < K) sk = __ldcg(slots + threadIdx.x);
+    float hv[8 * GPL];
 #pragma unroll
     for (int q = 0; q < 2 * GPL; ++q) {
-        const float4 v = reinterpret_cast<const float4 *>(h + (size_t)k * I + sl * 8 * GPL)[q];
-        hp[2 * q] = pack2(__float_as_uint(v.x), __float_as_uint(v.y));
-        hp[2 * q + 1] = pack2(__float_as_uint(v.z), __float_as_uint(v.w));
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(h + (size_t)k * I + sl * 8 * GPL) + q);
+        hv[4 * q] = v.x; hv[4 * q + 1] = v.y; hv[4 * q + 2] = v.z; hv[4 * q + 3] = v.w;
+    }
+    if (flag <= layer) return;
+    const bool bad = threadIdx.x < K && (sk == 0 || (sk & 15));
+    if (bad) dev_error(ctrl, sk == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN);
+    if (__syncthreads_or(bad)) return;
+    if (threadIdx.x < 32) {
+        // kDnRows rows of I values start on a block boundary (kDnRows * I % 2048 == 0)
+        const uint32_t bytes = (uint32_t)matrix_bytes(kDnRows, I);
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, bytes * K);
+        __syncwarp();
+        if (threadIdx.x < K) {
+            const size_t off = 2 * matrix_bytes(I, H) + matrix_bytes(r0, I);
+            bulk_g2s(tiles + threadIdx.x * lay.tileb, reinterpret_cast<const uint8_t *>(sk) + off, bytes, bar);
+        }
     }
     pdl_trigger();
     if (!mbar_wait(bar, 0)) {
@@ -232,20 +281,16 @@ __global__ void dec_down_kernel(const uint64_t *__restrict__ slots, const float 
     const uint4 *tabc = tab + (lane & (kTabCopies - 1));
     const uint8_t *tile = tiles + k * lay.tileb;
 #pragma unroll 2
-    for (int rr = sub; rr < kDnRows; rr += kRowsPerPass) {
+    for (int rr = r_lo + sub; rr < r_lo + kDnRows / 2; rr += kRowsPerPass) {
         const int gtile = rr * (I / 8) + sl * GPL;  // group index inside the tile
         const uint8_t *blk = tile + (gtile >> 5) * kBlockBytes;
         const int g0 = gtile & 31;
-        unsigned long long a0 = 0, a1 = 0;
+        float ae = 0.f, ao = 0.f;
 #pragma unroll
-        for (int g = 0; g < GPL; g += 2) {
-            a0 = group_fma(*reinterpret_cast<const uint16_t *>(blk + 2 + 2 * (g0 + g)), &hp[4 * g], tabc, a0);
-            if (g + 1 < GPL)
-                a1 = group_fma(*reinterpret_cast<const uint16_t *>(blk + 4 + 2 * (g0 + g)), &hp[4 * (g + 1)], tabc,
-                               a1);
-        }
+        for (int g = 0; g < GPL; ++g)
+            group_fma_s(*reinterpret_cast<const uint16_t *>(blk + 2 + 2 * (g0 + g)), &hv[8 * g], tabc, ae, ao);
         const float d = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
-        const float o = group_sum<LPR>(d * (hsum2(a0) + hsum2(a1)));
+        const float o = group_sum<LPR>(d * (ae + ao));
         if (sl == 0) o_s[k * kDnRows + rr] = o;
     }
     __syncthreads();
@@ -257,19 +302,19 @@ __global__ void dec_down_kernel(const uint64_t *__restrict__ slots, const float 
     }
 }
 
-template <int GPL>
+template <int GPL, int SPLIT>
 static rl_status launch_gateup(const float *x, float eps, const uint64_t *slots, const int8_t *cb, float *h,
                                int32_t *ctrl, int layer, int H, int I, int K, cudaStream_t s) {
     const int U = gu_unit(H);
     const int G = std::min(sm_count(), K * I / U);
     const GuLayout lay(H, I, K, G);
-    if ((size_t)U * lay.rowb % 16 != 0 || lay.total > 200 * 1024 || (K * I) % U != 0)
+    if ((size_t)U * lay.rowb % 16 != 0 || lay.total > 200 * 1024 || (K * I) % U != 0 || G < K)
         return fail(RL_ERR_UNSUPPORTED, "moe_decode: gate/up tile geometry (H=%d, I=%d, K=%d)", H, I, K);
     if (eps >= 0.f)
-        return launch_pdl(dec_gateup_kernel<GPL, true>, dim3(G), dim3(kGuThreads), lay.total, s,
+        return launch_pdl(dec_gateup_kernel<GPL, SPLIT, true>, dim3(G), dim3(kGuThreads), lay.total, s,
                           "moe_decode gate/up", x, eps, slots, cb, h, ctrl, layer, H, I, K);
-    return launch_pdl(dec_gateup_kernel<GPL, false>, dim3(G), dim3(kGuThreads), lay.total, s, "moe_decode gate/up",
-                      x, eps, slots, cb, h, ctrl, layer, H, I, K);
+    return launch_pdl(dec_gateup_kernel<GPL, SPLIT, false>, dim3(G), dim3(kGuThreads), lay.total, s,
+                      "moe_decode gate/up", x, eps, slots, cb, h, ctrl, layer, H, I, K);
 }
 
 template <int GPL, int LPR>
@@ -278,7 +323,7 @@ static rl_status launch_down(const uint64_t *slots, const float *w, const int8_t
     const DnLayout lay(I, K);
     if (matrix_bytes(kDnRows, I) % 16 != 0 || (kDnRows * I) % 2048 != 0 || lay.total > 200 * 1024)
         return fail(RL_ERR_UNSUPPORTED, "moe_decode: down tile geometry (I=%d, K=%d)", I, K);
-    return launch_pdl(dec_down_kernel<GPL, LPR>, dim3(H / kDnRows), dim3(32 * K), lay.total, s, "moe_decode down",
+    return launch_pdl(dec_down_kernel<GPL, LPR>, dim3(H / kDnRows), dim3(64 * K), lay.total, s, "moe_decode down",
                       slots, w, cb, h, y, acc, ctrl, layer, H, I, K);
 }
 
@@ -308,10 +353,10 @@ extern "C" rl_status moe_decode(const rl_moe_shape *shp, int32_t layer, const fl
     float *h = static_cast<float *>(ws);
     cudaStream_t s = as_stream(stream);
     switch (H) {
-        case 256: st = launch_gateup<1>(xn, norm_eps, slots, codebook, h, ctrl, layer, H, I, K, s); break;
-        case 512: st = launch_gateup<2>(xn, norm_eps, slots, codebook, h, ctrl, layer, H, I, K, s); break;
-        case 1024: st = launch_gateup<4>(xn, norm_eps, slots, codebook, h, ctrl, layer, H, I, K, s); break;
-        default: st = launch_gateup<8>(xn, norm_eps, slots, codebook, h, ctrl, layer, H, I, K, s); break;
+        case 256: st = launch_gateup<1, 1>(xn, norm_eps, slots, codebook, h, ctrl, layer, H, I, K, s); break;
+        case 512: st = launch_gateup<2, 1>(xn, norm_eps, slots, codebook, h, ctrl, layer, H, I, K, s); break;
+        case 1024: st = launch_gateup<2, 2>(xn, norm_eps, slots, codebook, h, ctrl, layer, H, I, K, s); break;
+        default: st = launch_gateup<4, 2>(xn, norm_eps, slots, codebook, h, ctrl, layer, H, I, K, s); break;
     }
     if (st != RL_OK) return st;
     switch (I) {  // I/8 groups per row

@@ -27,11 +27,10 @@ __device__ __forceinline__ uint32_t bf16_bits(int v) {
 // codebook is first staged through `stage` (>= 2 KB of shared memory, reused afterwards) with
 // one coalesced load per thread, then expanded; ends with __syncthreads().
 __device__ __forceinline__ void build_pair_table(uint4 *tab, const int8_t *__restrict__ codebook, uint2 *stage) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) stage[i] = reinterpret_cast<const uint2 *>(codebook)[i];
-    __syncthreads();
-    for (int i = threadIdx.x; i < 256 * kTabCopies; i += blockDim.x) {
-        const int e = i / kTabCopies;
-        const uint2 raw = stage[e];
+    (void)stage;
+    // each entry is converted once (256 threads) and written to its 8 copies
+    for (int e = threadIdx.x; e < 256; e += blockDim.x) {
+        const uint2 raw = reinterpret_cast<const uint2 *>(codebook)[e];
         uint32_t w[4];
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
@@ -40,7 +39,10 @@ __device__ __forceinline__ void build_pair_table(uint4 *tab, const int8_t *__res
             const int g1 = (int8_t)((word >> (16 * (p & 1) + 8)) & 0xffu);
             w[p] = bf16_bits(g0) | (bf16_bits(g1) << 16);
         }
-        tab[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int c = 0; c < kTabCopies; ++c)  // rotated so one store instruction hits 8 bank quads
+            tab[e * kTabCopies + ((c + threadIdx.x) & (kTabCopies - 1))] = v;
     }
     __syncthreads();
 }
@@ -62,6 +64,25 @@ __device__ __forceinline__ float hsum2(unsigned long long a) {
 __device__ __forceinline__ unsigned long long signed_pair(uint32_t w, uint32_t s2, int shift) {
     const uint32_t ws = w ^ ((s2 << shift) & 0x80008000u);
     return pack2(ws << 16, ws & 0xffff0000u);
+}
+
+// Scalar-FMA form (measured slightly faster than the packed form on sm_103a): two
+// independent accumulators (even and odd values) per group.
+__device__ __forceinline__ void group_fma_s(uint32_t gs, const float *x, const uint4 *tabc, float &a_even,
+                                            float &a_odd) {
+    const uint4 q = tabc[(gs & 0xffu) * kTabCopies];
+    const uint32_t s = (gs >> 8) & 0xffu;
+    const uint32_t s2 = s | ((s << 15) & 0x007f0000u);
+    const uint32_t w0 = q.x ^ ((s2 << 15) & 0x80008000u), w1 = q.y ^ ((s2 << 13) & 0x80008000u);
+    const uint32_t w2 = q.z ^ ((s2 << 11) & 0x80008000u), w3 = q.w ^ ((s2 << 9) & 0x80008000u);
+    a_even = fmaf(__uint_as_float(w0 << 16), x[0], a_even);
+    a_odd = fmaf(__uint_as_float(w0 & 0xffff0000u), x[1], a_odd);
+    a_even = fmaf(__uint_as_float(w1 << 16), x[2], a_even);
+    a_odd = fmaf(__uint_as_float(w1 & 0xffff0000u), x[3], a_odd);
+    a_even = fmaf(__uint_as_float(w2 << 16), x[4], a_even);
+    a_odd = fmaf(__uint_as_float(w2 & 0xffff0000u), x[5], a_odd);
+    a_even = fmaf(__uint_as_float(w3 << 16), x[6], a_even);
+    a_odd = fmaf(__uint_as_float(w3 & 0xffff0000u), x[7], a_odd);
 }
 
 // acc += sum_{j<8} grid[idx][j] * (+-1)_j * x[j] for one group; `gs` = (idx | sign << 8),

@@ -17,7 +17,7 @@ rl_status prefill_check(const rl_moe_shape *shp, int32_t layer, int32_t T, const
     if (!offs || !ctrl || (T > 0 && (!xn || !pair_tok || !pair_k || !slots || !weights || !codebook || !y)))
         return fail(RL_ERR_INVALID, "%s: NULL required buffer", who);
     if ((long long)T * shp->top_k > (1ll << 30)) return fail(RL_ERR_UNSUPPORTED, "%s: too many pairs", who);
-    PrefillWs L(T, shp->hidden, shp->top_k, shp->inter);
+    PrefillWs L(T, shp->hidden, shp->top_k, shp->inter, shp->n_experts);
     if (T > 0 && (!ws || ws_bytes < L.total))
         return fail(RL_ERR_INVALID, "%s: workspace of %zu B needed, %zu given", who, L.total, ws_bytes);
     if ((reinterpret_cast<uintptr_t>(xn) | reinterpret_cast<uintptr_t>(ws) | reinterpret_cast<uintptr_t>(y)) & 15)
@@ -29,8 +29,9 @@ rl_status prefill_check(const rl_moe_shape *shp, int32_t layer, int32_t T, const
     uint8_t *w = static_cast<uint8_t *>(ws);
     a->hbuf = reinterpret_cast<float *>(w);
     a->outbuf = reinterpret_cast<float *>(w + L.h);
-    a->xb = reinterpret_cast<__nv_bfloat16 *>(w + L.h + L.out);
-    a->hb = reinterpret_cast<__nv_bfloat16 *>(w + L.h + L.out + L.xb);
+    a->xb16 = reinterpret_cast<uint16_t *>(w + L.h + L.out);
+    a->hb16 = reinterpret_cast<uint16_t *>(w + L.h + L.out + L.xb);
+    a->units = w + L.h + L.out + L.xb + L.hb;
     return RL_OK;
 }
 
@@ -68,5 +69,5 @@ rl_status launch_ordered_sum(const PrefillArgs &a, cudaStream_t s) {
 
 extern "C" size_t moe_prefill_workspace_bytes(const rl_moe_shape *shp, int32_t T) {
     if (!shp || T < 0 || shp->hidden <= 0 || shp->top_k <= 0 || shp->inter <= 0) return 0;
-    return rl::PrefillWs(T, shp->hidden, shp->top_k, shp->inter).total;
+    return rl::PrefillWs(T, shp->hidden, shp->top_k, shp->inter, shp->n_experts).total;
 }

@@ -18,19 +18,22 @@ struct PrefillArgs {
     // workspace carve-up
     float *hbuf;              // [P][I]   f32 SwiGLU activations, pair order
     float *outbuf;            // [T*K][H] f32 expert outputs, indexed by (token, k)
-    __nv_bfloat16 *xb;        // [T][H]   bf16 copy of xn (tensor-core path)
-    __nv_bfloat16 *hb;        // [P][I]   bf16 activations (tensor-core path)
+    uint16_t *xb16;           // [T][H]   16-bit copy of xn (tensor-core path)
+    uint16_t *hb16;           // [P][I]   16-bit SwiGLU activations, pair order (tensor-core path)
+    void *units;              // tensor-core work-unit lists
 };
 
 struct PrefillWs {
-    size_t h, out, xb, hb, total;
-    PrefillWs(int T, int H, int K, int I) {
+    size_t h, out, xb, hb, units, total;
+    PrefillWs(int T, int H, int K, int I, int E) {
         const size_t P = (size_t)T * K;
         h = align_up(P * I * sizeof(float), 256);
         out = align_up(P * H * sizeof(float), 256);
         xb = align_up((size_t)T * H * 2, 256);
         hb = align_up(P * I * 2, 256);
-        total = h + out + xb + hb;
+        // unit lists: at most (P / 64 + E) token blocks x (I / 64 gate/up + H / 128 down) row tiles
+        units = align_up(256 + 4 * (P / 64 + (size_t)E) * ((size_t)I / 64 + (size_t)H / 128), 256);
+        total = h + out + xb + hb + units;
     }
 };
 

@@ -7,7 +7,11 @@ sum + residual), x <- x + MoE(RMSNorm(x))).  Each token reads 590.6 MB of weight
 L2 (129 MB), so no L2 flush is needed between tokens.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode_stack|decode_layer]
+                    [--workload decode_stack|decode_layer] [--no-prefill] [--no-bounded]
+
+Besides the decode line it reports, at N=1, the 512-token prefill chunk ("prefill": tokens/s,
+tensor-core TFLOP/s and weight GB/s of moe_prefill_chunk) and the 48-layer, 2048-token chunk
+with bounded residency ("prefill_bounded": tokens/s with and without the host fills).
 
 Prints ONE JSON line (rank 0).  Multi-GPU: one process per GPU (torchrun); every rank decodes
 its own tokens (no collective on the data path, weak scaling); the line reports the whole-job
@@ -355,10 +359,103 @@ def run_ours(a):
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches_per_token * T * a.steps,
                 "us_per_token": ms_max * 1e3 / (T * a.steps)}
+        if ws == 1 and not a.no_prefill:
+            del model
+            torch.cuda.empty_cache()
+            line["prefill"] = prefill_leg(dev, a.steps, a.warmup)
+            if not a.no_bounded:
+                torch.cuda.empty_cache()
+                line["prefill_bounded"] = bounded_leg(dev, max(1, a.steps // 3), 1)
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def prefill_leg(dev, steps: int, warmup: int, path: str = "tc"):
+    """The 512-token prefill chunk (one layer, 512 experts, 5120 pairs): routing, pair build,
+    grouped expert GEMMs and the ordered combine, timed with events on the launching stream."""
+    import torch
+
+    import synth
+    from quantized_moe_expert_rl_gb300 import _lib as L
+    from quantized_moe_expert_rl_gb300 import engine
+    w = synth.WORKLOADS["prefill_chunk"]
+    model = engine.Model(w, device=dev)
+    T = w.tokens
+    b = engine.PrefillBuffers.make(model, T)
+    x = torch.from_numpy(synth.tokens(w)).to(dev)
+    y = torch.zeros_like(x)
+    stream = torch.cuda.Stream(device=dev)
+    fn = engine._experts_fn(path)
+
+    def full():
+        engine.enqueue_prefill_route(model, b, 0, x, stacked=False)
+        engine.enqueue_prefill_experts(model, b, 0, x, y, stacked=False, path=path)
+
+    def experts_only():
+        fn(model.shape, 0, T, x, b.offs, b.pair_tok, b.pair_k, b.slots, b.weights, model.codebook, y, 0, b.ctrl,
+           b.ws, b.ws.numel(), stream)
+
+    res = {}
+    with torch.cuda.stream(stream):
+        for name, f in (("path", full), ("experts", experts_only)):
+            for _ in range(warmup):
+                f()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                f()
+            e1.record(stream)
+            stream.synchronize()
+            res[name] = e0.elapsed_time(e1) / steps
+    assert b.ctrl.tolist() == [L.RL_NO_EARLY_OUT, 0], b.ctrl.tolist()
+    union = int((b.offs[1:] - b.offs[:-1] > 0).sum().item())
+    P = T * w.top_k
+    flops = 2.0 * P * 3 * w.hidden * w.inter
+    bytes_ = union * w.record_bytes
+    t_ex = res["experts"] * 1e-3
+    return {"workload": "prefill_chunk (1 layer, 512 tokens, 5120 pairs)", "operands": "bf16" if path == "tc" else "f32",
+            "tokens_per_s": T / (res["path"] * 1e-3), "ms_per_chunk": res["path"],
+            "experts_ms_per_chunk": res["experts"], "experts_tokens_per_s": T / t_ex,
+            "experts_tflops": flops / t_ex / 1e12, "experts_hbm_gbs": bytes_ / t_ex / 1e9,
+            "union_experts": union, "flop_per_chunk": flops, "weight_bytes_per_chunk": bytes_}
+
+
+def bounded_leg(dev, steps: int, warmup: int, path: str = "tc"):
+    """48 layers x 2048 tokens with Zipf router bias and 85% residency: every step runs the
+    chunk from the seeded residency (fills from pinned host memory on each early-out)."""
+    import time
+
+    import torch
+
+    import synth
+    from quantized_moe_expert_rl_gb300 import engine
+    w = synth.WORKLOADS["prefill_bounded"]
+    model = engine.Model(w, device=dev)
+    b = engine.PrefillBuffers.make(model, w.tokens)
+    x0 = torch.from_numpy(synth.tokens(w)).to(dev)
+    x = torch.empty_like(x0)
+    walls, fills, last = [], [], None
+    for i in range(warmup + steps):
+        model.reset_residency()
+        x.copy_(x0)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        st = engine.run_bounded_chunk(model, b, x, path=path)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        if i >= warmup:
+            walls.append(wall)
+            fills.append(st.fill_seconds)
+            last = st
+    wall = sum(walls) / len(walls)
+    fill = sum(fills) / len(fills)
+    return {"workload": "prefill_bounded (48 layers x 2048 tokens, Zipf 1.1, 435/512 resident)",
+            "tokens_per_s_excl_fill": w.tokens / (wall - fill), "tokens_per_s_incl_fill": w.tokens / wall,
+            "s_per_chunk": wall, "fill_s_per_chunk": fill, "early_outs": len(last.early_outs),
+            "first_early_out": last.first_early_out, "misses_total": sum(last.miss),
+            "experts_filled": len(last.filled), "fill_bytes": last.fill_bytes, "host_syncs": last.syncs}
 
 
 def main():
@@ -371,6 +468,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--ref-step-s", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-bounded", action="store_true")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -45,6 +45,16 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    """Dense bf16 tensor-core peak in TFLOP/s: the measured burst figure (the chunk's GEMMs are
+    timed alone), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(p))["bf16_tflops"]), "measured bf16_tflops"
+    except Exception:
+        return 1900.0, "fallback bf16_tflops"
+
+
 def _src_digest() -> str:
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "quantized_moe_expert_rl_gb300", "csrc")
@@ -415,7 +425,15 @@ def prefill_leg(dev, steps: int, warmup: int, path: str = "tc"):
     flops = 2.0 * P * 3 * w.hidden * w.inter
     bytes_ = union * w.record_bytes
     t_ex = res["experts"] * 1e-3
+    hbm, hbm_kind = _peaks()
+    tf, tf_kind = _tensor_peak()
+    t_hbm, t_tc = bytes_ / (hbm * 1e9), flops / (tf * 1e12)
+    roof = {"bound": "hbm" if t_hbm >= t_tc else "tensor", "kernel": "moe_prefill_chunk (tc_gemm gate/up + down)",
+            "achieved_gbs": bytes_ / t_ex / 1e9, "peak_gbs": hbm, "frac_hbm": t_hbm / t_ex,
+            "achieved_tflops": flops / t_ex / 1e12, "peak_tflops": tf, "frac_tensor": t_tc / t_ex,
+            "traffic": _traffic("tc_gemm", 1.0), "peak_source": f"{hbm_kind} hbm_gbs, {tf_kind}"}
     return {"workload": "prefill_chunk (1 layer, 512 tokens, 5120 pairs)", "operands": "bf16" if path == "tc" else "f32",
+            "roofline": roof,
             "tokens_per_s": T / (res["path"] * 1e-3), "ms_per_chunk": res["path"],
             "experts_ms_per_chunk": res["experts"], "experts_tokens_per_s": T / t_ex,
             "experts_tflops": flops / t_ex / 1e12, "experts_hbm_gbs": bytes_ / t_ex / 1e9,

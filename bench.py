@@ -216,12 +216,16 @@ def run_reference(a):
 
 
 def _config(w, a):
-    return {"workload": w.name, "hidden": w.hidden, "n_experts": w.n_experts, "top_k": w.top_k,
-            "inter": w.inter, "n_layers": w.n_layers, "tokens_per_step": w.tokens,
-            "record_bytes": w.record_bytes, "resident_bytes": w.n_layers * w.n_experts * w.record_bytes,
+    nl = getattr(a, "layers", None) or w.n_layers
+    c = {"workload": w.name if nl == w.n_layers else f"{w.name} (first {nl} layers)", "hidden": w.hidden,
+         "n_experts": w.n_experts, "top_k": w.top_k, "inter": w.inter, "n_layers": nl, "tokens_per_step": w.tokens,
+         "record_bytes": w.record_bytes, "resident_bytes": nl * w.n_experts * w.record_bytes,
             "l2": "inputs larger than L2 (590.6 MB of weights per token)" if w.n_layers > 1 else
                   "per-token working set 12.3 MB (router stays L2-resident across tokens)",
             "parallelism": f"replicas x{a.gpus}", "seed": w.seed}
+    if w.n_layers > 1:
+        c["decode_path"] = getattr(a, "decode_path", "fused")
+    return c
 
 
 # ------------------------------------------------------------------------------------------
@@ -246,7 +250,7 @@ def run_ours(a):
     w = synth.WORKLOADS[a.workload]
     stacked = w.n_layers > 1
     T = w.tokens
-    model = engine.Model(w, device=dev)
+    model = engine.Model(w, device=dev, layers=a.layers)
     b = engine.DecodeBuffers.make(model)
     # this rank's tokens (weak scaling: every rank decodes its own 256 / 1000 tokens)
     x_host = torch.from_numpy(synth.tokens(w, rank * T, T)).pin_memory()
@@ -254,20 +258,33 @@ def run_ours(a):
     y_out = torch.zeros_like(x_in)
     y_host = torch.empty_like(x_host).pin_memory()
     stream = torch.cuda.Stream(device=dev)
-    with torch.cuda.stream(stream):
-        engine.enqueue_decode_token(model, b, x_in[0], y_out[0], stacked)
-    stream.synchronize()
-    graphs = []
-    for t in range(T):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            engine.enqueue_decode_token(model, b, x_in[t], y_out[t], stacked)
-        graphs.append(g)
-    launches_per_token = model.L * 3          # rl_route: 1 kernel; moe_decode: 2 kernels
+    fused = stacked and a.decode_path == "fused"
 
-    def step():
-        for g in graphs:
-            g.replay()
+    if fused:
+        # one moe_decode_stack launch per token runs all layers (plus the copy of x into y)
+        def token(t):
+            engine.enqueue_decode_token_fused(model, b, x_in[t], y_out[t])
+        launches_per_token = 1
+
+        def step():
+            for t in range(T):
+                token(t)
+    else:
+        # per-token CUDA graphs of the per-layer chain: rl_route (1 kernel) + moe_decode (2)
+        with torch.cuda.stream(stream):
+            engine.enqueue_decode_token(model, b, x_in[0], y_out[0], stacked)
+        stream.synchronize()
+        graphs = []
+        for t in range(T):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                engine.enqueue_decode_token(model, b, x_in[t], y_out[t], stacked)
+            graphs.append(g)
+        launches_per_token = model.L * 3
+
+        def step():
+            for g in graphs:
+                g.replay()
 
     def barrier():
         if ws > 1:
@@ -295,7 +312,7 @@ def run_ours(a):
     ms_max = float(t_max.item())
     value = ws * T * a.steps / (ms_max / 1e3)
 
-    # ---- end to end: pinned host x -> device, the token graphs, device -> pinned host y ----
+    # ---- end to end: pinned host x -> device, the tokens, device -> pinned host y ----
     h2d = x_host.numel() * 4
     d2h = y_host.numel() * 4
     barrier()
@@ -313,46 +330,73 @@ def run_ours(a):
         dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
     e2e_value = ws * T * a.steps / (float(e2e_ms.item()) / 1e3)
 
-    # ---- dominant call: moe_decode (expert gate/up GEMV + down GEMV with ordered combine) ----
-    # Timed alone per launch with events on its stream, over sampled tokens x all layers, the
-    # slots of each (token, layer) recorded first from the real chain.
-    kt_tokens = min(T, 16)
-    slots_rec = torch.zeros((kt_tokens, model.L, w.top_k), dtype=torch.int64, device=dev)
-    w_rec = torch.zeros((kt_tokens, model.L, w.top_k), dtype=torch.float32, device=dev)
-    xs_rec = torch.zeros((kt_tokens, model.L, w.hidden), dtype=torch.float32, device=dev)
-    with torch.cuda.stream(stream):
-        for t in range(kt_tokens):
-            engine.enqueue_decode_token(model, b, x_in[t], y_out[t], stacked, x_hist=xs_rec[t] if stacked else None)
-            slots_rec[t].copy_(b.slots)
-            w_rec[t].copy_(b.weights)
-            if not stacked:
-                xs_rec[t, 0].copy_(x_in[t])
-    stream.synchronize()
-    ybuf = torch.zeros(w.hidden, dtype=torch.float32, device=dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(kt_tokens * model.L)]
-    eps = engine.EPS if stacked else -1.0
-    with torch.cuda.stream(stream):
-        for rep in range(2):                      # first pass warms the code path
-            i = 0
-            for t in range(kt_tokens):
-                for l in range(model.L):
-                    s_, e_ = evs[i]
-                    s_.record(stream)
-                    L.moe_decode(model.shape, l, xs_rec[t, l], eps, slots_rec[t, l], w_rec[t, l], model.codebook,
-                                 ybuf, 0, b.ctrl, b.dec_ws, b.dec_ws.numel(), stream)
-                    e_.record(stream)
-                    i += 1
-    stream.synchronize()
-    durs = np.array([s_.elapsed_time(e_) for s_, e_ in evs]) * 1e-3      # seconds
-    t_launch = float(np.mean(durs))
-    bytes_per_launch = (w.top_k * w.record_bytes + 2 * w.hidden * 4 + 2 * w.top_k * w.inter * 4)
     peak, peak_kind = _peaks()
-    achieved = bytes_per_launch / t_launch / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": _traffic("moe_decode", 1.0), "kernel": "moe_decode (gate/up + down GEMVs)",
-                "bytes_per_launch": bytes_per_launch, "launch_us": t_launch * 1e6,
-                "peak_source": f"{peak_kind} hbm_gbs"}
+    per_layer_bytes = w.top_k * w.record_bytes + w.n_experts * w.hidden * 4 + 2 * w.hidden * 4
+    kt_tokens = min(T, 16)
+    if fused:
+        # ---- dominant kernel: moe_decode_stack, one launch = one token through every layer ----
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(kt_tokens)]
+        ybuf = torch.zeros(w.hidden, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            for rep in range(2):                  # first pass warms the code path
+                for t in range(kt_tokens):
+                    ybuf.copy_(x_in[t])
+                    s_, e_ = evs[t]
+                    s_.record(stream)
+                    L.moe_decode_stack(model.shape, 0, model.L, ybuf, engine.EPS, model.routers, model.bias,
+                                       model.table, model.codebook, b.ids, b.weights, b.slots, b.miss, b.ctrl,
+                                       None, None, b.stack_ws, b.stack_ws.numel(), stream)
+                    e_.record(stream)
+        stream.synchronize()
+        durs = np.array([s_.elapsed_time(e_) for s_, e_ in evs]) * 1e-3
+        t_launch = float(np.mean(durs))
+        bytes_per_launch = model.L * per_layer_bytes
+        achieved = bytes_per_launch / t_launch / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": _traffic("moe_decode_stack", 1.0),
+                    "kernel": f"moe_decode_stack ({model.L} layers of router + experts per launch)",
+                    "bytes_per_launch": bytes_per_launch, "launch_us": t_launch * 1e6,
+                    "us_per_layer": t_launch * 1e6 / model.L, "peak_source": f"{peak_kind} hbm_gbs"}
+    else:
+        # ---- dominant call: moe_decode (expert gate/up GEMV + down GEMV with ordered combine) ----
+        # Timed alone per launch with events on its stream, over sampled tokens x all layers, the
+        # slots of each (token, layer) recorded first from the real chain.
+        slots_rec = torch.zeros((kt_tokens, model.L, w.top_k), dtype=torch.int64, device=dev)
+        w_rec = torch.zeros((kt_tokens, model.L, w.top_k), dtype=torch.float32, device=dev)
+        xs_rec = torch.zeros((kt_tokens, model.L, w.hidden), dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            for t in range(kt_tokens):
+                engine.enqueue_decode_token(model, b, x_in[t], y_out[t], stacked, x_hist=xs_rec[t] if stacked else None)
+                slots_rec[t].copy_(b.slots)
+                w_rec[t].copy_(b.weights)
+                if not stacked:
+                    xs_rec[t, 0].copy_(x_in[t])
+        stream.synchronize()
+        ybuf = torch.zeros(w.hidden, dtype=torch.float32, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(kt_tokens * model.L)]
+        eps = engine.EPS if stacked else -1.0
+        with torch.cuda.stream(stream):
+            for rep in range(2):                      # first pass warms the code path
+                i = 0
+                for t in range(kt_tokens):
+                    for l in range(model.L):
+                        s_, e_ = evs[i]
+                        s_.record(stream)
+                        L.moe_decode(model.shape, l, xs_rec[t, l], eps, slots_rec[t, l], w_rec[t, l],
+                                     model.codebook, ybuf, 0, b.ctrl, b.dec_ws, b.dec_ws.numel(), stream)
+                        e_.record(stream)
+                        i += 1
+        stream.synchronize()
+        durs = np.array([s_.elapsed_time(e_) for s_, e_ in evs]) * 1e-3      # seconds
+        t_launch = float(np.mean(durs))
+        bytes_per_launch = (w.top_k * w.record_bytes + 2 * w.hidden * 4 + 2 * w.top_k * w.inter * 4)
+        achieved = bytes_per_launch / t_launch / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": _traffic("moe_decode", 1.0), "kernel": "moe_decode (gate/up + down GEMVs)",
+                    "bytes_per_launch": bytes_per_launch, "launch_us": t_launch * 1e6,
+                    "peak_source": f"{peak_kind} hbm_gbs"}
 
     line = None
     if rank == 0:
@@ -488,6 +532,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-bounded", action="store_true")
+    ap.add_argument("--decode-path", choices=["fused", "chain"], default="fused",
+                    help="stacked decode: one moe_decode_stack launch per token, or per-token graphs of the "
+                         "per-layer rl_route + moe_decode chain")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers of the stacked workload (profiling of smaller cases)")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -173,6 +173,38 @@ rl_status moe_decode_static(const rl_moe_shape *shp, int32_t layer, const float 
                             int32_t accumulate, int32_t *ctrl, void *stream);
 
 /*
+ * moe_decode_stack - a run of layers [layer0, layer0 + n_layers) of ONE token in a single
+ * launch: for each layer l, the work of rl_route(l) then moe_decode(l) on the residual stream
+ *   xn = RMSNorm(x) (norm_eps >= 0; norm_eps < 0: xn = x),  route as rl_route,
+ *   x <- x + sum_{k in order} weights[l][k] * down_k(silu(gate_k xn) * (up_k xn)).
+ * "Red Lite dev38 - decode: expert down-projection lanes and concurrent encoders", "Finding":
+ * serialization between the small per-layer kernels was the dominant waste; here the layers
+ * meet at on-chip grid barriers instead of kernel boundaries.  "Red Lite dev21", "What
+ * changed": no host round trip between router and experts.  "Red Lite dev23", "What changed",
+ * item 1: at the first layer f that selects an absent expert, ids/weights/slots[f] and miss[f]
+ * are written, ctrl[0] = min(ctrl[0], f), and the launch stops with x = x_f (the input of
+ * layer f), so the caller can fill, rl_resolve_slots(f), moe_decode(f) and resume at f + 1.
+ * Results are bit-identical to the per-layer chain rl_route + moe_decode (same arithmetic).
+ * x [H] f32 in/out (16-byte aligned); w_router [n_layers][E][H] f32; bias [n_layers][E] f32 or
+ * NULL; residency [n_layers][E]; codebook int8 [256][8]; ids int32, weights f32, slots uint64:
+ * [n_layers][K] (rows of the run are written); miss uint32 [n_layers] (accumulated);
+ * logits_out f32 [n_layers][E] or NULL; x_hist f32 [n_layers][H] or NULL (x_l, the input of
+ * each layer run, for validation).  Does nothing when ctrl[0] < layer0.
+ * ws: moe_decode_stack_workspace_bytes(shp) bytes, 16-byte aligned, zero-filled before its
+ * first use; it holds a grid-barrier counter that grows across calls, so calls sharing one
+ * workspace must not overlap on the GPU, and after a call that raised RL_DEVERR_WAIT_TIMEOUT
+ * it must be zero-filled again.  One CTA runs on every SM (cooperative launch); a shape whose
+ * CTA does not fit an SM returns RL_ERR_UNSUPPORTED before any launch.  Every on-chip wait is
+ * bounded: on expiry RL_DEVERR_WAIT_TIMEOUT is set in ctrl[1] and the launch ends.
+ */
+size_t moe_decode_stack_workspace_bytes(const rl_moe_shape *shp);
+rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x, float norm_eps,
+                           const float *w_router, const float *bias, const uint64_t *residency,
+                           const int8_t *codebook, int32_t *ids, float *weights, uint64_t *slots,
+                           uint32_t *miss, int32_t *ctrl, float *logits_out, float *x_hist, void *ws,
+                           size_t ws_bytes, void *stream);
+
+/*
  * rl_build_pairs - (expert, token) pairs sorted by expert, stable in (t, k) order
  * ("Red Lite dev20", "What changed", item 3):
  *   offs[e] .. offs[e+1]-1 index the pairs of expert e; pair p is (pair_tok[p], pair_k[p]).

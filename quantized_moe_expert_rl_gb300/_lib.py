@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "RL_OK", 1: "RL_ERR_INVALID", 2: "RL_ERR_UNSUPPORTED", 3: "RL
 EXPORTS = ("rl_abi_version", "rl_last_error", "rl_record_bytes", "rl_rmsnorm", "rl_route_workspace_bytes",
            "rl_route", "rl_resolve_slots", "moe_decode_workspace_bytes", "moe_decode",
            "rl_build_pairs_workspace_bytes", "rl_build_pairs", "moe_prefill_workspace_bytes",
-           "moe_prefill_chunk", "moe_prefill_chunk_f32", "moe_decode_static")
+           "moe_prefill_chunk", "moe_prefill_chunk_f32", "moe_decode_static", "moe_decode_stack_workspace_bytes",
+           "moe_decode_stack")
 
 
 class RlShape(ctypes.Structure):
@@ -64,6 +65,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_decode_workspace_bytes": (sz, [shp]),
         "moe_decode": (i32, [shp, i32, vp, f32, vp, vp, vp, vp, i32, vp, vp, sz, vp]),
         "moe_decode_static": (i32, [shp, i32, vp, f32, vp, vp, vp, vp, i32, vp, vp]),
+        "moe_decode_stack_workspace_bytes": (sz, [shp]),
+        "moe_decode_stack": (i32, [shp, i32, i32, vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "rl_build_pairs_workspace_bytes": (sz, [shp, i32]),
         "rl_build_pairs": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_prefill_workspace_bytes": (sz, [shp, i32]),
@@ -144,6 +147,18 @@ def moe_decode_static(shape, layer, x, norm_eps, slots, weights, codebook, y, ac
     _check("moe_decode_static", load().moe_decode_static(ctypes.byref(shape), layer, ptr(x), float(norm_eps),
                                                          ptr(slots), ptr(weights), ptr(codebook), ptr(y),
                                                          int(accumulate), ptr(ctrl), _stream(stream)))
+
+
+def moe_decode_stack_workspace_bytes(shape) -> int:
+    return load().moe_decode_stack_workspace_bytes(ctypes.byref(shape))
+
+
+def moe_decode_stack(shape, layer0, n_layers, x, norm_eps, w_router, bias, residency, codebook, ids, weights, slots,
+                     miss, ctrl, logits_out, x_hist, ws, ws_bytes, stream=None):
+    _check("moe_decode_stack", load().moe_decode_stack(
+        ctypes.byref(shape), layer0, n_layers, ptr(x), float(norm_eps), ptr(w_router), ptr(bias), ptr(residency),
+        ptr(codebook), ptr(ids), ptr(weights), ptr(slots), ptr(miss), ptr(ctrl), ptr(logits_out), ptr(x_hist),
+        ptr(ws), ws_bytes, _stream(stream)))
 
 
 def rl_build_pairs_workspace_bytes(shape, T) -> int:

@@ -20,17 +20,12 @@
 #include <algorithm>
 #include <mutex>
 
-#include "qdot.cuh"
+#include "decode_rows.cuh"
 
 namespace rl {
 
 constexpr int kGuThreads = 1024;
 constexpr int kDnRows = 16;
-
-// rows of the flat (expert, row) space handled together so that copies stay 16-byte multiples
-__host__ __device__ inline int gu_unit(int H) { return H >= 2048 ? 1 : 2048 / H; }
-// warps per row: wide rows are split in two halves so that a lane holds only 32 inputs
-__host__ __device__ inline int gu_split(int H) { return H >= 1024 ? 2 : 1; }
 
 constexpr int kGuChunks = 4;  // row chunks per expert segment, each with its own mbarrier
 
@@ -47,20 +42,6 @@ struct GuLayout {
         total = 128 + kTabBytes + (size_t)H * sizeof(float) + part + tiles;
     }
 };
-
-// Partial (gate, up) dots of one lane for one row pair.
-template <int GPL>
-__device__ __forceinline__ void gu_row(const uint8_t *gb, const uint8_t *ub, int g0, const float *xv,
-                                       const uint4 *tabc, float &gv, float &uv) {
-    float ge = 0.f, go = 0.f, ue = 0.f, uo = 0.f;
-#pragma unroll
-    for (int g = 0; g < GPL; ++g) {
-        group_fma_s(*reinterpret_cast<const uint16_t *>(gb + 2 + 2 * (g0 + g)), &xv[8 * g], tabc, ge, go);
-        group_fma_s(*reinterpret_cast<const uint16_t *>(ub + 2 + 2 * (g0 + g)), &xv[8 * g], tabc, ue, uo);
-    }
-    gv = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(gb)) * (ge + go);
-    uv = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(ub)) * (ue + uo);
-}
 
 // GPL = groups (8 values) per lane = H / (256 * SPLIT); SPLIT warps per (gate, up) row pair.
 template <int GPL, int SPLIT, bool NORM>
@@ -165,7 +146,7 @@ __global__ void __launch_bounds__(kGuThreads) dec_gateup_kernel(const float *__r
         while (c + 1 < kGuChunks && r >= cut(seg, c + 1)) ++c;
         const int bi = seg * kGuChunks + c;
         if (!(ready & (1u << bi))) {
-            if (!mbar_wait(&bars[bi], 0)) timed_out = true;
+            if (!mbar_wait_warp(&bars[bi], 0)) timed_out = true;
             ready |= 1u << bi;
         }
         gb = tiles + (seg == 0 ? 0 : 2 * (size_t)n0 * lay.rowb) + (size_t)r * lay.rowb + boff;
@@ -209,11 +190,7 @@ __global__ void __launch_bounds__(kGuThreads) dec_gateup_kernel(const float *__r
     }
     __syncthreads();
     if (timed_out) return;
-    for (int t = threadIdx.x; t < p1 - p0; t += blockDim.x) {
-        float gv = part[t * 4 + 0], uv = part[t * 4 + 1];
-        if (SPLIT == 2) { gv += part[t * 4 + 2]; uv += part[t * 4 + 3]; }
-        h[p0 + t] = silu(gv) * uv;  // p = k * I + i
-    }
+    for (int t = threadIdx.x; t < p1 - p0; t += blockDim.x) h[p0 + t] = swiglu_part<SPLIT>(part + 4 * t);  // p = k*I + i
 }
 
 struct DnLayout {
@@ -274,7 +251,7 @@ __global__ void dec_down_kernel(const uint64_t *__restrict__ slots, const float 
         }
     }
     pdl_trigger();
-    if (!mbar_wait(bar, 0)) {
+    if (!mbar_wait_warp(bar, 0)) {
         if (lane == 0) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
         return;
     }
@@ -282,22 +259,13 @@ __global__ void dec_down_kernel(const uint64_t *__restrict__ slots, const float 
     const uint8_t *tile = tiles + k * lay.tileb;
 #pragma unroll 2
     for (int rr = r_lo + sub; rr < r_lo + kDnRows / 2; rr += kRowsPerPass) {
-        const int gtile = rr * (I / 8) + sl * GPL;  // group index inside the tile
-        const uint8_t *blk = tile + (gtile >> 5) * kBlockBytes;
-        const int g0 = gtile & 31;
-        float ae = 0.f, ao = 0.f;
-#pragma unroll
-        for (int g = 0; g < GPL; ++g)
-            group_fma_s(*reinterpret_cast<const uint16_t *>(blk + 2 + 2 * (g0 + g)), &hv[8 * g], tabc, ae, ao);
-        const float d = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
-        const float o = group_sum<LPR>(d * (ae + ao));
+        const float o = down_row<GPL, LPR>(tile, rr, I, sl, hv, tabc);
         if (sl == 0) o_s[k * kDnRows + rr] = o;
     }
     __syncthreads();
     if (threadIdx.x < kDnRows) {
         const int r = r0 + threadIdx.x;
-        float acc = 0.f;
-        for (int kk = 0; kk < K; ++kk) acc = acc + weights[kk] * o_s[kk * kDnRows + threadIdx.x];
+        const float acc = ordered_combine(weights, o_s + threadIdx.x, kDnRows, K);
         y[r] = (accumulate ? y[r] : 0.f) + acc;
     }
 }
@@ -362,7 +330,7 @@ extern "C" rl_status moe_decode(const rl_moe_shape *shp, int32_t layer, const fl
     switch (I) {  // I/8 groups per row
         case 128: return launch_down<1, 16>(slots, weights, codebook, h, y, accumulate, ctrl, layer, H, I, K, s);
         case 256: return launch_down<1, 32>(slots, weights, codebook, h, y, accumulate, ctrl, layer, H, I, K, s);
-        case 512: return launch_down<2, 32>(slots, weights, codebook, h, y, accumulate, ctrl, layer, H, I, K, s);
+        case 512: return launch_down<4, 16>(slots, weights, codebook, h, y, accumulate, ctrl, layer, H, I, K, s);
         case 1024: return launch_down<4, 32>(slots, weights, codebook, h, y, accumulate, ctrl, layer, H, I, K, s);
         default: return launch_down<8, 32>(slots, weights, codebook, h, y, accumulate, ctrl, layer, H, I, K, s);
     }

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kPfThreads) pf32_gateup_kernel(const float *__
     for (int i = threadIdx.x; i < kGridBytes / 8; i += blockDim.x)
         reinterpret_cast<uint2 *>(grid_s)[i] = reinterpret_cast<const uint2 *>(codebook)[i];
     __syncthreads();
-    if (!mbar_wait(bar, 0)) {
+    if (!mbar_wait_warp(bar, 0)) {
         if (threadIdx.x == 0) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
         return;
     }
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kPfThreads) pf32_down_kernel(const uint32_t *_
     for (int i = threadIdx.x; i < kGridBytes / 8; i += blockDim.x)
         reinterpret_cast<uint2 *>(grid_s)[i] = reinterpret_cast<const uint2 *>(codebook)[i];
     __syncthreads();
-    if (!mbar_wait(bar, 0)) {
+    if (!mbar_wait_warp(bar, 0)) {
         if (threadIdx.x == 0) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
         return;
     }

@@ -118,6 +118,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// The same wait made by lane 0 of the warp alone while the other lanes park in __syncwarp, so
+// that a waiting warp does not keep the shared-memory pipe busy with polls (which slows the
+// warps that compute).  Call with the whole warp; the result is warp-uniform.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+    return __shfl_sync(kFull, ok, 0) != 0;
+}
 // Contiguous copy of `bytes` (multiple of 16, both addresses 16-byte aligned) into shared
 // memory; completion is signalled as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {

@@ -15,74 +15,9 @@
 // CTA to finish (completion counter) selects, looks up and writes the outputs.
 // Many tokens (prefill): f32 tiled GEMM, then one warp per token selects.
 #include "qdot.cuh"
+#include "select.cuh"
 
 namespace rl {
-
-// ---------------------------------------------------------------------------------------------
-// Selection: one warp.  Lane l holds experts l*C .. l*C+C-1 (C = candidates per lane), so a
-// lower lane always holds lower expert indices.  Keys are the f32 logits mapped to
-// order-preserving uint32 after folding -0.0 into +0.0 (so the two compare equal); key 0 is
-// below every finite value and marks a taken or absent candidate.  Each round takes the warp
-// maximum with redux.sync; among equal keys the lowest lane wins, and inside a lane the first
-// (lowest) index wins, so ties go to the lower expert index.
-// ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t order_key(float v) {
-    const uint32_t b = __float_as_uint(v + 0.0f);  // -0.0 + 0.0 = +0.0
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-template <int C>
-__device__ __forceinline__ void warp_select(const float *lg, const uint64_t *__restrict__ table_row,
-                                            int32_t *ids, float *weights, uint64_t *slots, uint32_t *miss_l,
-                                            int32_t *ctrl, int layer, int E, int K) {
-    const int lane = threadIdx.x & 31;
-    uint32_t key[C];
-    uint32_t best = 0u;
-    int bi = 0;
-#pragma unroll
-    for (int i = 0; i < C; ++i) {
-        const int e = lane * C + i;
-        key[i] = e < E ? order_key(__ldcg(lg + e)) : 0u;
-        if (key[i] > best) { best = key[i]; bi = i; }
-    }
-    int my_id = 0;
-    float my_val = 0.f;
-    for (int r = 0; r < K; ++r) {
-        const uint32_t m = __reduce_max_sync(kFull, best);
-        const int wl = __ffs(__ballot_sync(kFull, best == m)) - 1;
-        const int wi = __shfl_sync(kFull, bi, wl);
-        if (lane == r) { my_id = wl * C + wi; my_val = key_value(m); }
-        if (lane == wl) {  // the winner drops its candidate and finds its next best
-            best = 0u;
-            bi = 0;
-#pragma unroll
-            for (int i = 0; i < C; ++i) {
-                if (i == wi) key[i] = 0u;
-                if (key[i] > best) { best = key[i]; bi = i; }
-            }
-        }
-    }
-    // w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0), the sum taken in selection order
-    const float l0 = __shfl_sync(kFull, my_val, 0);
-    const float ex = lane < K ? expf(my_val - l0) : 0.f;
-    float tot = 0.f;
-    for (int k = 0; k < K; ++k) tot += __shfl_sync(kFull, ex, k);
-    uint64_t slot = 1;
-    if (lane < K) {
-        ids[lane] = my_id;
-        weights[lane] = ex / tot;
-        slot = table_row[my_id];
-        slots[lane] = slot;
-    }
-    const int nmiss = __popc(__ballot_sync(kFull, lane < K && slot == 0));
-    if (lane == 0 && nmiss > 0) {
-        atomicAdd(miss_l, (uint32_t)nmiss);
-        atomicMin(ctrl, layer);
-    }
-}
 
 // ---------------------------------------------------------------------------------------------
 // RMSNorm: one CTA per token; warp 0 computes the deterministic scale, all threads apply it.
@@ -145,7 +80,7 @@ __global__ void __launch_bounds__(kR1Threads) route1_kernel(const float *__restr
     }
     __syncthreads();
     // the router rows must have landed before the CTA may exit, whether it skips or not
-    if (!mbar_wait(bar, 0)) {
+    if (!mbar_wait_warp(bar, 0)) {
         if (threadIdx.x == 0) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
         return;
     }

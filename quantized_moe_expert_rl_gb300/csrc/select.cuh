@@ -1,0 +1,155 @@
+// select.cuh - top-k selection of one token's router logits by one warp, with the
+// renormalised weights ("Red Lite dev21 - GPU-routed decode", "What changed": rl_route picks
+// the top-k by logit, ties to the lower index, and renormalises the weights over the
+// selection).  Shared by rl_route and the fused decode stack so both select identically.
+//
+// Lane l holds experts l*C .. l*C+C-1 (C = candidates per lane), so a lower lane always holds
+// lower expert indices.  Keys are the f32 logits mapped to order-preserving uint32 after
+// folding -0.0 into +0.0 (so the two compare equal); key 0 is below every finite value and
+// marks a taken or absent candidate.  Each round takes the warp maximum with redux.sync; among
+// equal keys the lowest lane wins, and inside a lane the first (lowest) index wins, so ties go
+// to the lower expert index.
+#pragma once
+#include "rl_common.cuh"
+
+namespace rl {
+
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t b = __float_as_uint(v + 0.0f);  // -0.0 + 0.0 = +0.0
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// After the call lane r < K holds the r-th selected expert (my_id) and its logit (my_val).
+// The logits are read through L2 (they may come from other CTAs).
+template <int C>
+__device__ __forceinline__ void warp_topk(const float *lg, int E, int K, int &my_id, float &my_val) {
+    const int lane = threadIdx.x & 31;
+    uint32_t key[C];
+    uint32_t best = 0u;
+    int bi = 0;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+        const int e = lane * C + i;
+        key[i] = e < E ? order_key(__ldcg(lg + e)) : 0u;
+        if (key[i] > best) { best = key[i]; bi = i; }
+    }
+    my_id = 0;
+    my_val = 0.f;
+    for (int r = 0; r < K; ++r) {
+        const uint32_t m = __reduce_max_sync(kFull, best);
+        const int wl = __ffs(__ballot_sync(kFull, best == m)) - 1;
+        const int wi = __shfl_sync(kFull, bi, wl);
+        if (lane == r) { my_id = wl * C + wi; my_val = key_value(m); }
+        if (lane == wl) {  // the winner drops its candidate and finds its next best
+            best = 0u;
+            bi = 0;
+#pragma unroll
+            for (int i = 0; i < C; ++i) {
+                if (i == wi) key[i] = 0u;
+                if (key[i] > best) { best = key[i]; bi = i; }
+            }
+        }
+    }
+}
+
+// w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0), the sum taken in selection order; lane k < K
+// gets w_k (other lanes 0).
+__device__ __forceinline__ float topk_weight(float my_val, int K) {
+    const int lane = threadIdx.x & 31;
+    const float l0 = __shfl_sync(kFull, my_val, 0);
+    const float ex = lane < K ? expf(my_val - l0) : 0.f;
+    float tot = 0.f;
+    for (int k = 0; k < K; ++k) tot += __shfl_sync(kFull, ex, k);
+    return lane < K ? ex / tot : 0.f;
+}
+
+// Full rl_route selection for one token: ids, weights, slots, miss count and flag.
+template <int C>
+__device__ __forceinline__ void warp_select(const float *lg, const uint64_t *__restrict__ table_row,
+                                            int32_t *ids, float *weights, uint64_t *slots, uint32_t *miss_l,
+                                            int32_t *ctrl, int layer, int E, int K) {
+    const int lane = threadIdx.x & 31;
+    int my_id;
+    float my_val;
+    warp_topk<C>(lg, E, K, my_id, my_val);
+    const float w = topk_weight(my_val, K);
+    uint64_t slot = 1;
+    if (lane < K) {
+        ids[lane] = my_id;
+        weights[lane] = w;
+        slot = table_row[my_id];
+        slots[lane] = slot;
+    }
+    const int nmiss = __popc(__ballot_sync(kFull, lane < K && slot == 0));
+    if (lane == 0 && nmiss > 0) {
+        atomicAdd(miss_l, (uint32_t)nmiss);
+        atomicMin(ctrl, layer);
+    }
+}
+
+}  // namespace rl
+
+namespace rl {
+
+// Top-k of up to 32 * NW logits with NW warps of one CTA (the fused decode stack runs it in
+// every CTA).  Level 1: warp w owns experts 32w .. 32w+31 (lane = expert within the warp) and
+// takes its own top-k by K rounds of warp max, the lowest lane winning among equal keys, so
+// each warp's list is ordered by (logit descending, index ascending).  The residency-table
+// entry of every expert is loaded together with its logit.  Level 2 (warp 0): a K-round merge
+// of the NW lists, lane j holding the head of list j; equal keys go to the lowest list, whose
+// experts have the lower indices.  The result (ids, logits and their table entries) is the
+// same as warp_topk's, since both follow the one total order (logit descending, index
+// ascending).  cand_key/cand_id/cand_slot: shared scratch of NW * K entries.  Lane r < K of
+// warp 0 ends with the r-th selection; the CTA is converged on return.
+template <int NW>
+__device__ __forceinline__ void cta_topk(const float *lg, const uint64_t *__restrict__ table_row, int E, int K,
+                                         uint32_t *cand_key, int *cand_id, uint64_t *cand_slot, int &my_id,
+                                         float &my_val, uint64_t &my_slot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp < NW) {
+        const int e = warp * 32 + lane;
+        uint32_t key = 0u;
+        uint64_t slot = 0;
+        if (e < E) {
+            key = order_key(__ldcg(lg + e));
+            slot = __ldcg(table_row + e);
+        }
+        for (int r = 0; r < K; ++r) {
+            const uint32_t m = __reduce_max_sync(kFull, key);
+            const int wl = __ffs(__ballot_sync(kFull, key == m)) - 1;
+            if (lane == wl) {
+                cand_key[warp * K + r] = m;
+                cand_id[warp * K + r] = e;
+                cand_slot[warp * K + r] = slot;
+                key = 0u;
+            }
+        }
+    }
+    __syncthreads();
+    my_id = 0;
+    my_val = 0.f;
+    my_slot = 0;
+    if (warp == 0) {
+        int ptr = 0;
+        uint32_t hk = lane < NW ? cand_key[lane * K] : 0u;
+        for (int r = 0; r < K; ++r) {
+            const uint32_t m = __reduce_max_sync(kFull, hk);
+            const int wl = __ffs(__ballot_sync(kFull, hk == m)) - 1;
+            const int at = __shfl_sync(kFull, wl * K + ptr, wl);
+            if (lane == r) {
+                my_id = cand_id[at];
+                my_val = key_value(m);
+                my_slot = cand_slot[at];
+            }
+            if (lane == wl) {
+                ++ptr;
+                hk = (ptr < K && lane < NW) ? cand_key[lane * K + ptr] : 0u;
+            }
+        }
+    }
+}
+
+}  // namespace rl

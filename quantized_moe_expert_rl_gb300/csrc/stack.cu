@@ -1,0 +1,556 @@
+// stack.cu - the fused decode stack: ONE persistent kernel runs a run of layers of one token,
+//   x <- x + sum_{k in order} w_k * down_k(silu(gate_k xn) * (up_k xn)),  xn = RMSNorm(x),
+// with the router, the selection, the residency lookup, the miss count and the early-out flag
+// of every layer inside the same launch.
+//
+// Red Lite dev38 - decode lanes, "Finding": on the pages' GPU the serialization between the
+// many small decode kernels, not the bandwidth of any one of them, was the dominant waste.
+// Red Lite dev21 - GPU-routed decode, "What changed": no host round trip sits between the
+// router and the experts.  Red Lite dev23 - per-layer early-out, "What changed" item 1: the
+// layer that selects a non-resident expert raises the flag and nothing after it runs.
+//
+// Design: one CTA per SM (cooperative launch, so all CTAs are co-resident), 16 warps each.
+// Every CTA owns a fixed slice of each phase's work for the whole launch:
+//   router rows [e0, e0+nr), gate/up (expert, row) pairs [p0, p1), down output rows [q0, q0+nq).
+// Per layer:
+//   A  x_l (L2) -> RMSNorm scale; logits of the CTA's router rows, whose weights were copied
+//      into shared memory during the previous layer (they do not depend on x);
+//      grid barrier
+//   B  every CTA selects the top-k from all logits itself (the same code on the same data
+//      gives the same ids everywhere, so no further exchange is needed); CTA 0 writes the
+//      outputs, the miss count and the flag; a miss (or the flag) stops every CTA.  Then the
+//      CTA's gate/up rows and down rows of the K selected experts are copied into shared
+//      memory with bulk asynchronous copies, all at once;
+//   C  gate/up + SwiGLU of the CTA's pairs -> h (L2); the next layer's router rows are
+//      requested;  grid barrier
+//   D  the CTA's rows of every expert's down projection, the ordered combine and the
+//      residual -> x_{l+1} (L2);  grid barrier.
+// The arithmetic of every row, the RMSNorm scale and the selection are the very functions the
+// per-layer kernels (rl_route, moe_decode) use, so the result is bit-identical to that chain.
+//
+// Grid barrier: a 64-bit arrival counter in the workspace that only ever grows.  The first
+// arrival of a launch rounds its value down to a multiple of the grid size to find the base,
+// so no reset is needed between launches.  Every spin is bounded: on expiry the CTA sets
+// RL_DEVERR_WAIT_TIMEOUT, waits (bounded) for its own copies in flight and returns; the other
+// CTAs then time out at their next barrier.
+#include "decode_rows.cuh"
+#include "select.cuh"
+
+namespace rl {
+
+constexpr int kStThreads = 512;
+constexpr int kStWarps = kStThreads / 32;
+constexpr int kStGuChunks = 2;
+constexpr int kStBars = 2 + 2 * kStGuChunks;  // [0] router rows, [1] down rows, [2..] gate/up chunks
+constexpr uint32_t kSpinCap = 1u << 22;       // global-memory polls (~1 us each): seconds
+constexpr int kStSelWarps = 16;               // selection warps: E <= 32 * 16
+constexpr int kStHdr = 4608;                  // barriers, scalars, CTA constants, selection scratch
+// The warp that issues every bulk copy.  A memory fence waits for the bulk copies its own
+// thread has in flight, so the thread that runs the grid barrier (thread 0) never issues one.
+constexpr int kStProducer = kStWarps - 1;
+
+// down rows handled together so that every copy starts on a block boundary (rows * I % 2048 == 0)
+__host__ __device__ inline int dn_unit(int I) { return I >= 2048 ? 1 : 2048 / I; }
+
+struct StLayout {
+    int rt_max, rmax, dmax, rowb, dtileb;
+    size_t o_x, o_rt, o_part, o_gu, o_dn, o_o, total;
+    __host__ __device__ StLayout(int H, int E, int K, int I, int G) {
+        rt_max = (E + G - 1) / G;
+        const int U = gu_unit(H), units = K * I / U;
+        rmax = ((units + G - 1) / G) * U;
+        const int Ud = dn_unit(I), gq = H / Ud;
+        dmax = ((gq + G - 1) / G) * Ud;
+        rowb = (int)matrix_bytes(1, H);
+        dtileb = (int)align_up(matrix_bytes(dmax, I), 16);
+        o_x = kStHdr + kTabBytes;
+        o_rt = o_x + (size_t)H * sizeof(float);
+        o_part = o_rt + (size_t)rt_max * H * sizeof(float);
+        o_gu = o_part + align_up((size_t)rmax * 4 * sizeof(float), 16);
+        o_dn = o_gu + 2 * (size_t)rmax * rowb;
+        o_o = o_dn + (size_t)K * dtileb;
+        total = o_o + (size_t)K * dmax * sizeof(float);
+    }
+};
+
+// This CTA's fixed share of every phase and its shared-memory layout, kept in shared memory
+// (read where needed) so that the layer loop keeps few registers live.
+struct StCta {
+    int e0, nr;              // router rows
+    int p0, p1, ka, kb, n0, n1;  // gate/up (expert, row) pairs: two segments (experts ka, kb)
+    int q0, nq;              // down output rows
+    int rowb, dtileb, dmax;
+    uint32_t o_x, o_rt, o_part, o_gu, o_dn, o_o;
+};
+
+struct StackArgs {
+    float *x;
+    float eps;
+    const float *W;          // [L][E][H]
+    const float *bias;       // [L][E] or NULL
+    const uint64_t *table;   // [L][E]
+    const int8_t *codebook;  // [256][8]
+    int32_t *ids;            // [L][K]
+    float *weights;          // [L][K]
+    uint64_t *slots;         // [L][K]
+    uint32_t *miss;          // [L]
+    int32_t *ctrl;
+    float *logits_out;  // [L][E] or NULL
+    float *x_hist;      // [L][H] or NULL
+    unsigned long long *ctr;
+    float *lg;  // [E]
+    float *h;   // [K][I]
+    int layer0, nl, H, E, K, I;
+};
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// All CTAs of the grid meet; writes before it (through L2) are visible after it.  Thread 0
+// keeps the barrier target in a register; `target` = 0 means "not yet based".
+__device__ __forceinline__ bool grid_sync(unsigned long long *ctr, unsigned long long &target, int *ok_s,
+                                          int32_t *ctrl) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned long long old = atomicAdd(ctr, 1ull);
+        if (target == 0ull) target = old - old % gridDim.x + 1ull;  // +1 marks "based"
+        target += gridDim.x;
+        bool ok = false;
+        for (uint32_t i = 0; i < kSpinCap; ++i)
+            if (ld_acquire_u64(ctr) >= target - 1ull) {
+                ok = true;
+                break;
+            }
+        if (!ok) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
+        __threadfence();
+        *ok_s = ok;
+    }
+    __syncthreads();
+    return *ok_s != 0;
+}
+
+// chunk c of gate/up segment `seg` holds rows [cut, cut') of the segment
+__device__ __forceinline__ int gu_cut(const StCta &c, int U, int seg, int ch) {
+    return ((seg == 0 ? c.n0 : c.n1) / U * ch / kStGuChunks) * U;
+}
+
+// NV = H / 128 float4 router columns per lane; GPL, SPLIT: gate/up lane geometry (moe_decode);
+// DGPL, LPR: down lane geometry.
+template <int NV, int GPL, int SPLIT, int DGPL, int LPR>
+__global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *bar_rt = bars, *bar_dn = bars + 1, *bar_gu = bars + 2;
+    float *scale_s = reinterpret_cast<float *>(smem + 64);
+    int *stop_s = reinterpret_cast<int *>(smem + 68);
+    int *ok_s = reinterpret_cast<int *>(smem + 72);
+    StCta &C = *reinterpret_cast<StCta *>(smem + 128);
+    uint64_t *slots_s = reinterpret_cast<uint64_t *>(smem + 256);
+    float *w_s = reinterpret_cast<float *>(smem + 384);
+    uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem + 512);
+    int *cand_id = reinterpret_cast<int *>(smem + 1536);
+    uint64_t *cand_slot = reinterpret_cast<uint64_t *>(smem + 2560);
+    uint4 *tab = reinterpret_cast<uint4 *>(smem + kStHdr);
+    constexpr int H = NV * 128;
+    constexpr int U = H >= 2048 ? 1 : 2048 / H;  // gu_unit(H)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    if (threadIdx.x == 0) {
+        const int E = a.E, K = a.K, I = a.I, G = gridDim.x, b = blockIdx.x;
+        const StLayout lay(H, E, K, I, G);
+        C.e0 = (int)((long long)b * E / G);
+        C.nr = (int)((long long)(b + 1) * E / G) - C.e0;
+        const int units = K * I / U;
+        C.p0 = (int)((long long)b * units / G) * U;
+        C.p1 = (int)((long long)(b + 1) * units / G) * U;
+        const bool has = C.p1 > C.p0;
+        C.ka = has ? C.p0 / I : 0;
+        C.kb = has ? (C.p1 - 1) / I : 0;
+        C.n0 = has ? (C.ka == C.kb ? C.p1 : (C.ka + 1) * I) - C.p0 : 0;
+        C.n1 = (C.p1 - C.p0) - C.n0;
+        const int Ud = dn_unit(I), gq = H / Ud;
+        C.q0 = (int)((long long)b * gq / G) * Ud;
+        C.nq = (int)((long long)(b + 1) * gq / G) * Ud - C.q0;
+        C.rowb = lay.rowb;
+        C.dtileb = lay.dtileb;
+        C.dmax = lay.dmax;
+        C.o_x = (uint32_t)lay.o_x; C.o_rt = (uint32_t)lay.o_rt; C.o_part = (uint32_t)lay.o_part;
+        C.o_gu = (uint32_t)lay.o_gu; C.o_dn = (uint32_t)lay.o_dn; C.o_o = (uint32_t)lay.o_o;
+        for (int i = 0; i < kStBars; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    build_pair_table(tab, a.codebook, nullptr);  // ends with __syncthreads
+    const int flag0 = ld_ctrl(a.ctrl);
+    if (flag0 < a.layer0) return;  // an earlier layer already stopped the chain
+
+    // one thread: this CTA's router rows of layer l into shared memory
+    auto issue_router = [&](int l) {
+        const uint32_t bytes = (uint32_t)((size_t)C.nr * H * sizeof(float));
+        mbar_arrive_expect_tx(bar_rt, bytes);
+        bulk_g2s(smem + C.o_rt, a.W + ((size_t)l * a.E + C.e0) * H, bytes, bar_rt);
+    };
+    if (threadIdx.x == kStProducer * 32 && C.nr > 0) issue_router(a.layer0);
+
+    unsigned long long target = 0;  // grid barrier state (thread 0)
+    // copies in flight, for the exit path: parity of the router copy (-1: none) and whether
+    // this layer's expert copies were issued
+    int rt_par = C.nr > 0 ? 0 : -1;
+    bool ex_issued = false;
+    bool failed = false;
+    uint32_t ph = 0;
+    for (int i = 0; i < a.nl; ++i, ph ^= 1u) {
+        const int l = a.layer0 + i;
+        const bool last = i + 1 == a.nl;
+        ex_issued = false;
+        // ---------------- A: x_l, its scale, this CTA's logits ----------------
+        {
+            float *x_s = reinterpret_cast<float *>(smem + C.o_x);
+            for (int j = threadIdx.x; j < H / 4; j += kStThreads)
+                reinterpret_cast<float4 *>(x_s)[j] = __ldcg(reinterpret_cast<const float4 *>(a.x) + j);
+            __syncthreads();
+            if (warp == 0) {
+                const float r = a.eps >= 0.f ? rms_scale_warp(x_s, H, a.eps) : 1.f;
+                if (lane == 0) *scale_s = r;
+            }
+            if (a.x_hist && blockIdx.x == 0)
+                for (int j = threadIdx.x; j < H; j += kStThreads) a.x_hist[(size_t)l * H + j] = x_s[j];
+            const int nr = C.nr;
+            if (warp < nr && !mbar_wait_warp(bar_rt, ph)) failed = true;
+            __syncthreads();
+            if (warp < nr && !failed) {
+                const float4 *xr = reinterpret_cast<const float4 *>(x_s);
+                const float4 *wr = reinterpret_cast<const float4 *>(smem + C.o_rt) + (size_t)warp * (H / 4);
+                const bool norm = a.eps >= 0.f;
+                const float r = *scale_s;
+                unsigned long long a0 = 0, a1 = 0;
+#pragma unroll
+                for (int j = 0; j < NV; ++j) {
+                    float4 v = xr[lane + 32 * j];
+                    if (norm) { v.x *= r; v.y *= r; v.z *= r; v.w *= r; }
+                    const float4 w = wr[lane + 32 * j];
+                    a0 = ffma2(pack2(__float_as_uint(w.x), __float_as_uint(w.y)),
+                               pack2(__float_as_uint(v.x), __float_as_uint(v.y)), a0);
+                    a1 = ffma2(pack2(__float_as_uint(w.z), __float_as_uint(w.w)),
+                               pack2(__float_as_uint(v.z), __float_as_uint(v.w)), a1);
+                }
+                const float s = warp_sum(hsum2(a0) + hsum2(a1));
+                if (lane == 0) {
+                    const int e = C.e0 + warp;
+                    const float lv = s + (a.bias ? a.bias[(size_t)l * a.E + e] : 0.f);
+                    __stcg(a.lg + e, lv);
+                    if (a.logits_out) a.logits_out[(size_t)l * a.E + e] = lv;
+                }
+            }
+        }
+        failed = __syncthreads_or(failed) != 0;
+        if (failed) break;
+        rt_par = -1;
+        if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
+
+        // ---------------- B: selection (the same in every CTA), expert copies ----------------
+        {
+            const int K = a.K;
+            int my_id;
+            float my_val;
+            uint64_t slot;
+            cta_topk<kStSelWarps>(a.lg, a.table + (size_t)l * a.E, a.E, K, cand_key, cand_id, cand_slot, my_id,
+                                  my_val, slot);
+            if (warp == 0) {
+                const float w = topk_weight(my_val, K);
+                const int nmiss = __popc(__ballot_sync(kFull, lane < K && slot == 0));
+                const bool bad = __ballot_sync(kFull, lane < K && slot != 0 && (slot & 15)) != 0;
+                if (lane < K) {
+                    slots_s[lane] = slot;
+                    w_s[lane] = w;
+                }
+                if (blockIdx.x == 0) {
+                    if (lane < K) {
+                        a.ids[(size_t)l * K + lane] = my_id;
+                        a.weights[(size_t)l * K + lane] = w;
+                        a.slots[(size_t)l * K + lane] = slot;
+                    }
+                    if (lane == 0 && nmiss > 0) {
+                        atomicAdd(a.miss + l, (uint32_t)nmiss);
+                        atomicMin(a.ctrl, l);
+                    }
+                    if (lane == 0 && bad) dev_error(a.ctrl, RL_DEVERR_SLOT_ALIGN);
+                }
+                const bool stop = nmiss > 0 || bad || flag0 <= l;
+                if (lane == 0) *stop_s = stop;
+            }
+        }
+        __syncthreads();
+        if (*stop_s) break;
+        if (warp == kStProducer) {
+            fence_proxy_async_smem();
+            const int K = a.K, I = a.I, rowb = C.rowb;
+            const size_t matb = matrix_bytes(I, H);
+            // gate/up: lane i < 2 * kStGuChunks issues chunk (segment i / kStGuChunks, part
+            // i % kStGuChunks): its gate rows and its up rows, completion on bar_gu[i]
+            if (lane < 2 * kStGuChunks && C.p1 > C.p0) {
+                const int seg = lane / kStGuChunks, ch = lane % kStGuChunks;
+                const int n = seg == 0 ? C.n0 : C.n1;
+                const int r0 = gu_cut(C, U, seg, ch), r1 = gu_cut(C, U, seg, ch + 1);
+                if (r1 > r0) {
+                    const uint8_t *base = reinterpret_cast<const uint8_t *>(slots_s[seg == 0 ? C.ka : C.kb]);
+                    const int ia = seg == 0 ? C.p0 - C.ka * I : 0;
+                    const uint32_t bytes = (uint32_t)((r1 - r0) * rowb);
+                    uint8_t *gdst = smem + C.o_gu + (seg == 0 ? 0 : 2 * (size_t)C.n0 * rowb) + (size_t)r0 * rowb;
+                    mbar_arrive_expect_tx(&bar_gu[lane], 2 * bytes);
+                    bulk_g2s(gdst, base + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
+                    bulk_g2s(gdst + (size_t)n * rowb, base + matb + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
+                }
+            }
+            // down: rows [q0, q0 + nq) of every selected expert, completion on bar_dn
+            const int nq = C.nq;
+            if (nq > 0) {
+                const uint32_t bytes = (uint32_t)matrix_bytes(nq, I);
+                if (lane == 0) mbar_arrive_expect_tx(bar_dn, bytes * K);
+                __syncwarp();
+                if (lane < K)
+                    bulk_g2s(smem + C.o_dn + (size_t)lane * C.dtileb,
+                             reinterpret_cast<const uint8_t *>(slots_s[lane]) + 2 * matb + matrix_bytes(C.q0, I), bytes,
+                             bar_dn);
+            }
+        }
+        ex_issued = true;
+
+        // ---------------- C: gate/up + SwiGLU of this CTA's pairs ----------------
+        if (C.p1 > C.p0) {
+            const int p0 = C.p0, p1 = C.p1, n0 = C.n0, n1 = C.n1, rowb = C.rowb;
+            const uint8_t *gtiles = smem + C.o_gu;
+            float *part = reinterpret_cast<float *>(smem + C.o_part);
+            const int half = warp % SPLIT, team = warp / SPLIT;
+            constexpr int kTeams = kStWarps / SPLIT;
+            const int c0 = half * (H / SPLIT) + lane * 8 * GPL;
+            float xv[8 * GPL];
+            {
+                const float r = *scale_s;
+                const float *x_s = reinterpret_cast<const float *>(smem + C.o_x);
+#pragma unroll
+                for (int q = 0; q < 2 * GPL; ++q) {
+                    const float4 v = reinterpret_cast<const float4 *>(x_s + c0)[q];
+                    xv[4 * q] = v.x * r; xv[4 * q + 1] = v.y * r; xv[4 * q + 2] = v.z * r; xv[4 * q + 3] = v.w * r;
+                }
+            }
+            const uint4 *tabc = tab + (lane & (kTabCopies - 1));
+            const int gl = c0 / 8, boff = (gl >> 5) * kBlockBytes, g0 = gl & 31;
+            unsigned ready = 0;
+            bool to = false;
+            auto locate = [&](int p, const uint8_t *&gb, const uint8_t *&ub) {
+                const int seg = p - p0 < n0 ? 0 : 1;
+                const int r = seg == 0 ? p - p0 : p - p0 - n0;
+                const int n = seg == 0 ? n0 : n1;
+                int ch = 0;
+                while (ch + 1 < kStGuChunks && r >= ((n / U) * (ch + 1) / kStGuChunks) * U) ++ch;
+                const int bi = seg * kStGuChunks + ch;
+                if (!(ready & (1u << bi))) {
+                    if (!mbar_wait_warp(&bar_gu[bi], ph)) to = true;
+                    ready |= 1u << bi;
+                }
+                gb = gtiles + (seg == 0 ? 0 : 2 * (size_t)n0 * rowb) + (size_t)r * rowb + boff;
+                ub = gb + (size_t)n * rowb;
+            };
+            for (int p = p0 + team; p < p1; p += 2 * kTeams) {
+                const int q = p + kTeams;  // second row pair in flight
+                const uint8_t *gb, *ub, *gb2 = nullptr, *ub2 = nullptr;
+                locate(p, gb, ub);
+                if (q < p1) locate(q, gb2, ub2);
+                if (to) break;
+                float gv, uv, gv2 = 0.f, uv2 = 0.f;
+                gu_row<GPL>(gb, ub, g0, xv, tabc, gv, uv);
+                if (q < p1) gu_row<GPL>(gb2, ub2, g0, xv, tabc, gv2, uv2);
+                gv = warp_sum(gv);
+                uv = warp_sum(uv);
+                gv2 = warp_sum(gv2);
+                uv2 = warp_sum(uv2);
+                if (lane == 0) {
+                    part[((p - p0) * 2 + half) * 2 + 0] = gv;
+                    part[((p - p0) * 2 + half) * 2 + 1] = uv;
+                    if (q < p1) {
+                        part[((q - p0) * 2 + half) * 2 + 0] = gv2;
+                        part[((q - p0) * 2 + half) * 2 + 1] = uv2;
+                    }
+                }
+            }
+            if (to) failed = true;
+        }
+        failed = __syncthreads_or(failed) != 0;
+        if (failed) break;
+        {
+            const int p0 = C.p0, np = C.p1 - C.p0;
+            const float *part = reinterpret_cast<const float *>(smem + C.o_part);
+            for (int t = threadIdx.x; t < np; t += kStThreads) __stcg(a.h + p0 + t, swiglu_part<SPLIT>(part + 4 * t));
+        }
+        // the router rows of the next layer (every warp is done with this layer's)
+        if (C.nr > 0 && !last) {
+            if (threadIdx.x == kStProducer * 32) {
+                fence_proxy_async_smem();
+                issue_router(l + 1);
+            }
+            rt_par = (int)(ph ^ 1u);
+        }
+        if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
+
+        // ---------------- D: down rows of every expert, ordered combine, residual ----------------
+        {
+            const int nq = C.nq, K = a.K;
+            if (nq > 0) {
+                const int wpe = kStWarps / K;  // warps per expert
+                constexpr int kRpp = 32 / LPR;   // rows per warp pass
+                const int k = warp / wpe, j = warp % wpe, sub = lane / LPR, sl = lane % LPR;
+                if (k < K) {
+                    const int I = a.I, dmax = C.dmax;
+                    float hv[8 * DGPL];
+#pragma unroll
+                    for (int q = 0; q < 2 * DGPL; ++q) {
+                        const float4 v =
+                            __ldcg(reinterpret_cast<const float4 *>(a.h + (size_t)k * I + sl * 8 * DGPL) + q);
+                        hv[4 * q] = v.x; hv[4 * q + 1] = v.y; hv[4 * q + 2] = v.z; hv[4 * q + 3] = v.w;
+                    }
+                    if (!mbar_wait_warp(bar_dn, ph)) {
+                        failed = true;
+                    } else {
+                        const uint4 *tabc = tab + (lane & (kTabCopies - 1));
+                        const uint8_t *tile = smem + C.o_dn + (size_t)k * C.dtileb;
+                        float *o_s = reinterpret_cast<float *>(smem + C.o_o);
+                        for (int rr = j * kRpp + sub; rr < nq; rr += wpe * kRpp) {
+                            const float o = down_row<DGPL, LPR>(tile, rr, I, sl, hv, tabc);
+                            if (sl == 0) o_s[k * dmax + rr] = o;
+                        }
+                    }
+                }
+            }
+        }
+        failed = __syncthreads_or(failed) != 0;
+        if (failed) break;
+        ex_issued = false;
+        if ((int)threadIdx.x < C.nq) {
+            const int r = C.q0 + threadIdx.x;
+            const float *o_s = reinterpret_cast<const float *>(smem + C.o_o);
+            const float *x_s = reinterpret_cast<const float *>(smem + C.o_x);
+            const float acc = ordered_combine(w_s, o_s + threadIdx.x, C.dmax, a.K);
+            __stcg(a.x + r, x_s[r] + acc);
+        }
+        if (!last && !grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
+    }
+    // ---- exit: no copy into this CTA's shared memory may still be in flight ----
+    if (threadIdx.x == 0) {
+        if (rt_par >= 0) mbar_wait(bar_rt, (uint32_t)rt_par);
+        if (ex_issued) {
+            if (C.nq > 0) mbar_wait(bar_dn, ph);
+            for (int bi = 0; bi < 2 * kStGuChunks; ++bi) {
+                const int seg = bi / kStGuChunks, ch = bi % kStGuChunks;
+                if (C.p1 > C.p0 && gu_cut(C, U, seg, ch + 1) > gu_cut(C, U, seg, ch)) mbar_wait(&bar_gu[bi], ph);
+            }
+        }
+    }
+    __syncthreads();
+}
+
+template <int NV, int GPL, int SPLIT, int DGPL, int LPR>
+static rl_status launch_stack(const StackArgs &a, cudaStream_t s) {
+    auto kern = stack_kernel<NV, GPL, SPLIT, DGPL, LPR>;
+    const int G = sm_count();
+    const StLayout lay(a.H, a.E, a.K, a.I, G);
+    if (lay.total > 227 * 1024 || lay.rt_max > kStWarps || lay.rmax > a.I || lay.dmax > kStThreads ||
+        kStWarps / a.K < 1)
+        return fail(RL_ERR_UNSUPPORTED, "moe_decode_stack: shape does not fit one CTA per SM (H=%d E=%d K=%d I=%d)",
+                    a.H, a.E, a.K, a.I);
+    rl_status st = allow_smem((const void *)kern, lay.total);
+    if (st != RL_OK) return st;
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kStThreads, lay.total);
+    if (e != cudaSuccess || occ < 1)
+        return fail(RL_ERR_UNSUPPORTED, "moe_decode_stack: no SM can hold the %zu B CTA", lay.total);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(kStThreads);
+    cfg.dynamicSmemBytes = lay.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return fail(RL_ERR_CUDA, "moe_decode_stack: launch failed: %s", cudaGetErrorString(e));
+    return RL_OK;
+}
+
+template <int NV, int GPL, int SPLIT>
+static rl_status launch_stack_i(const StackArgs &a, cudaStream_t s) {
+    switch (a.I) {
+        case 128: return launch_stack<NV, GPL, SPLIT, 1, 16>(a, s);
+        case 256: return launch_stack<NV, GPL, SPLIT, 1, 32>(a, s);
+        case 512: return launch_stack<NV, GPL, SPLIT, 4, 16>(a, s);
+        case 1024: return launch_stack<NV, GPL, SPLIT, 4, 32>(a, s);
+        default: return launch_stack<NV, GPL, SPLIT, 8, 32>(a, s);
+    }
+}
+
+}  // namespace rl
+
+using namespace rl;
+
+extern "C" size_t moe_decode_stack_workspace_bytes(const rl_moe_shape *shp) {
+    if (!shp || shp->n_experts <= 0 || shp->top_k <= 0 || shp->inter <= 0) return 0;
+    return 256 + align_up((size_t)shp->n_experts * sizeof(float), 256) +
+           align_up((size_t)shp->top_k * shp->inter * sizeof(float), 256);
+}
+
+extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x,
+                                      float norm_eps, const float *w_router, const float *bias,
+                                      const uint64_t *residency, const int8_t *codebook, int32_t *ids,
+                                      float *weights, uint64_t *slots, uint32_t *miss, int32_t *ctrl,
+                                      float *logits_out, float *x_hist, void *ws, size_t ws_bytes, void *stream) {
+    rl_status st = check_shape(shp);
+    if (st != RL_OK) return st;
+    if (layer0 < 0 || n_layers < 0 || layer0 + n_layers > shp->n_layers)
+        return fail(RL_ERR_INVALID, "moe_decode_stack: layers [%d, %d) outside [0, %d)", layer0, layer0 + n_layers,
+                    shp->n_layers);
+    if (!x || !w_router || !residency || !codebook || !ids || !weights || !slots || !miss || !ctrl)
+        return fail(RL_ERR_INVALID, "moe_decode_stack: NULL buffer");
+    if (!ws || ws_bytes < moe_decode_stack_workspace_bytes(shp))
+        return fail(RL_ERR_INVALID, "moe_decode_stack: workspace of %zu B needed, %zu given",
+                    moe_decode_stack_workspace_bytes(shp), ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router) | reinterpret_cast<uintptr_t>(ws) |
+         reinterpret_cast<uintptr_t>(x_hist)) & 15)
+        return fail(RL_ERR_INVALID, "moe_decode_stack: x, w_router, x_hist and ws must be 16-byte aligned");
+    if (n_layers == 0) return RL_OK;
+    StackArgs a;
+    a.x = x;
+    a.eps = norm_eps;
+    a.W = w_router;
+    a.bias = bias;
+    a.table = residency;
+    a.codebook = codebook;
+    a.ids = ids;
+    a.weights = weights;
+    a.slots = slots;
+    a.miss = miss;
+    a.ctrl = ctrl;
+    a.logits_out = logits_out;
+    a.x_hist = x_hist;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    a.ctr = reinterpret_cast<unsigned long long *>(w8);
+    a.lg = reinterpret_cast<float *>(w8 + 256);
+    a.h = reinterpret_cast<float *>(w8 + 256 + align_up((size_t)shp->n_experts * sizeof(float), 256));
+    a.layer0 = layer0;
+    a.nl = n_layers;
+    a.H = shp->hidden;
+    a.E = shp->n_experts;
+    a.K = shp->top_k;
+    a.I = shp->inter;
+    cudaStream_t s = as_stream(stream);
+    switch (a.H) {
+        case 256: return launch_stack_i<2, 1, 1>(a, s);
+        case 512: return launch_stack_i<4, 2, 1>(a, s);
+        case 1024: return launch_stack_i<8, 2, 2>(a, s);
+        default: return launch_stack_i<16, 4, 2>(a, s);
+    }
+}

@@ -142,6 +142,7 @@ class DecodeBuffers:
     ctrl: torch.Tensor       # [2] int32
     route_ws: torch.Tensor
     dec_ws: torch.Tensor
+    stack_ws: torch.Tensor   # zero-filled: grid-barrier counter of moe_decode_stack
 
     @staticmethod
     def make(model: Model) -> "DecodeBuffers":
@@ -157,7 +158,8 @@ class DecodeBuffers:
             miss=torch.zeros(Lh, dtype=torch.int32, device=d),
             ctrl=torch.tensor([RL_NO_EARLY_OUT, 0], dtype=torch.int32, device=d),
             route_ws=torch.zeros(max(256, L.rl_route_workspace_bytes(shp, 1)), dtype=torch.uint8, device=d),
-            dec_ws=torch.empty(L.moe_decode_workspace_bytes(shp), dtype=torch.uint8, device=d))
+            dec_ws=torch.empty(L.moe_decode_workspace_bytes(shp), dtype=torch.uint8, device=d),
+            stack_ws=torch.zeros(L.moe_decode_stack_workspace_bytes(shp), dtype=torch.uint8, device=d))
 
 
 def enqueue_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
@@ -187,6 +189,63 @@ def enqueue_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_o
         L.moe_decode(shp, l, b.x, EPS, b.slots[l], b.weights[l], model.codebook, b.x, 1, b.ctrl, b.dec_ws,
                      b.dec_ws.numel())
     y_out.copy_(b.x)
+
+
+def enqueue_decode_token_fused(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
+                               keep_logits: bool = False, x_hist: torch.Tensor | None = None,
+                               layer0: int = 0) -> None:
+    """Stacked decode of one token, layers [layer0, L), in ONE launch (moe_decode_stack):
+    y_out = x_in, then per layer y_out += MoE(RMSNorm(y_out)).  Bit-identical to
+    enqueue_decode_token(stacked=True).  x_hist[l] (optional) receives layer l's input."""
+    y_out.copy_(x_in)
+    L.moe_decode_stack(model.shape, layer0, model.L - layer0, y_out, EPS, model.routers, model.bias, model.table,
+                       model.codebook, b.ids, b.weights, b.slots, b.miss, b.ctrl, b.logits if keep_logits else None,
+                       x_hist, b.stack_ws, b.stack_ws.numel())
+
+
+@dataclass
+class DecodeStats:
+    early_outs: list        # layers at which the chain stopped for a fill
+    filled: list            # (layer, expert) filled
+    fill_bytes: int
+    syncs: int              # host reads of the control block
+
+
+def run_bounded_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
+                             x_hist: torch.Tensor | None = None) -> DecodeStats:
+    """One token through every layer with bounded residency ("Red Lite dev23", "What changed",
+    item 1): the fused stack runs until a layer f selects an absent expert and stops there
+    with y_out = x_f; the host reads the flag once, fills layer f's missing experts, re-resolves
+    its slots, runs layer f's experts with the ids and weights the GPU selected, and restarts
+    the stack at f + 1.  The caller zeroes b.miss; b.ctrl is reset here."""
+    shp, K = model.shape, model.w.top_k
+    b.ctrl.copy_(torch.tensor([RL_NO_EARLY_OUT, 0], dtype=torch.int32))
+    y_out.copy_(x_in)
+    st = DecodeStats([], [], 0, 0)
+    l0 = 0
+    while l0 < model.L:
+        L.moe_decode_stack(shp, l0, model.L - l0, y_out, EPS, model.routers, model.bias, model.table,
+                           model.codebook, b.ids, b.weights, b.slots, b.miss, b.ctrl, None, x_hist, b.stack_ws,
+                           b.stack_ws.numel())
+        ctrl = b.ctrl.tolist()
+        st.syncs += 1
+        if ctrl[1] != 0:
+            raise RuntimeError(f"moe_decode_stack: device error bits {ctrl[1]:#x}")
+        f = ctrl[0]
+        if f == RL_NO_EARLY_OUT:
+            break
+        ids = b.ids[f].tolist()
+        slots = b.slots[f].tolist()
+        missing = sorted({ids[k] for k in range(K) if slots[k] == 0})
+        st.fill_bytes += model.fill(f, missing)
+        st.filled += [(f, e) for e in missing]
+        st.early_outs.append(f)
+        L.rl_resolve_slots(shp, f, 1, b.ids[f], model.table, b.slots[f])
+        b.ctrl[0] = RL_NO_EARLY_OUT
+        L.moe_decode(shp, f, y_out, EPS, b.slots[f], b.weights[f], model.codebook, y_out, 1, b.ctrl, b.dec_ws,
+                     b.dec_ws.numel())
+        l0 = f + 1
+    return st
 
 
 @dataclass

@@ -208,3 +208,90 @@ def test_decode_early_out():
     assert b.miss.tolist() == [0, 2, 0]
     # layer 0 ran, layer 1's experts and layer 2 were skipped: the output is layer 1's input
     assert torch.equal(y[0], hist[1])
+
+
+def _bits(t):
+    t = t.detach().cpu().contiguous()
+    return t.view(torch.int32) if t.dtype == torch.float32 else t
+
+
+def test_decode_stack_fused_equals_chain(stack_model):
+    """moe_decode_stack (one launch per token for all 48 layers) against the per-layer chain
+    rl_route + moe_decode: logits, ids, weights, slots, every layer's input and the token's
+    output are bit-identical; the fused layers also match the oracle."""
+    engine = _engine()
+    w, m, o = stack_model
+    toks = [0, 77, w.tokens - 1]
+    x = torch.from_numpy(synth.tokens(w, 0, w.tokens)).cuda()
+    outs = {}
+    for mode in ("chain", "fused"):
+        b = engine.DecodeBuffers.make(m)
+        hist = torch.zeros((len(toks), m.L, w.hidden), device="cuda")
+        res = []
+        for i, t in enumerate(toks):
+            y = torch.zeros(w.hidden, device="cuda")
+            if mode == "chain":
+                engine.enqueue_decode_token(m, b, x[t], y, stacked=True, keep_logits=True, x_hist=hist[i])
+            else:
+                engine.enqueue_decode_token_fused(m, b, x[t], y, keep_logits=True, x_hist=hist[i])
+            torch.cuda.synchronize()
+            res.append([_bits(v) for v in (b.logits, b.ids, b.weights, b.slots, y)])
+        assert b.ctrl.tolist() == [0x7FFFFFFF, 0] and int(b.miss.sum()) == 0
+        outs[mode] = (res, _bits(hist), hist.double().cpu().numpy(), res[0][4].view(torch.float32).double().numpy())
+    for ra, rb in zip(outs["chain"][0], outs["fused"][0]):
+        for name, a_, b_ in zip(("logits", "ids", "weights", "slots", "y"), ra, rb):
+            assert torch.equal(a_, b_), name
+    assert torch.equal(outs["chain"][1], outs["fused"][1])
+    # the fused run of token 0 against the oracle, every 4th layer from its own layer inputs
+    H = outs["fused"][2][0]
+    y_last = outs["fused"][3]
+    rep = {}
+    for l in range(0, m.L, 4):
+        xn = oracle.rmsnorm(H[l:l + 1])
+        lg = outs["fused"][0][0][0].view(torch.float32).numpy()[l:l + 1]
+        ids = outs["fused"][0][0][1].numpy()[l:l + 1]
+        wts = outs["fused"][0][0][2].view(torch.float32).numpy()[l:l + 1]
+        sl = outs["fused"][0][0][3].numpy().view(np.uint64)[l:l + 1]
+        r = check_route(lg, ids, wts, sl, oracle.router_logits(xn, o.router(l)), o.table_row(l), w.top_k, l, rep)
+        y_o = o.experts(xn, r.ids, r.weights, r.slots)
+        x_next = H[l + 1] if l + 1 < m.L else y_last
+        assert rel_l2(x_next - H[l], y_o[0]) <= REL_F32, l
+
+
+def test_decode_stack_bounded_residency():
+    """Bounded residency through the fused stack: each token stops at the first layer that
+    selects an absent expert, with the exact miss count; the host fills that layer's missing
+    experts and resumes.  Outputs and selections equal those of a fully resident model bit
+    for bit, and the early-out layers follow from the selections and the residency."""
+    engine = _engine()
+    base = replace(synth.WORKLOADS["tiny"], n_layers=6)
+    wb = replace(base, n_resident=26)
+    m_full, m_b = engine.Model(base), engine.Model(wb)
+    b_full, b_b = engine.DecodeBuffers.make(m_full), engine.DecodeBuffers.make(m_b)
+    x = torch.from_numpy(synth.tokens(base, 0, base.tokens)).cuda()
+    resident = np.stack([synth.resident_mask(wb, l).astype(bool) for l in range(wb.n_layers)])
+    n_early = 0
+    for t in range(base.tokens):
+        y_full = torch.zeros(base.hidden, device="cuda")
+        y_b = torch.zeros(base.hidden, device="cuda")
+        engine.enqueue_decode_token_fused(m_full, b_full, x[t], y_full)
+        b_b.miss.zero_()
+        st = engine.run_bounded_decode_token(m_b, b_b, x[t], y_b)
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(y_full), _bits(y_b)), t
+        assert torch.equal(_bits(b_full.ids), _bits(b_b.ids)) and torch.equal(_bits(b_full.weights), _bits(b_b.weights))
+        ids = b_full.ids.cpu().numpy()
+        exp_miss, exp_early, exp_fill = [], [], []
+        for l in range(wb.n_layers):
+            miss = [int(e) for e in ids[l] if not resident[l, e]]
+            exp_miss.append(len(miss))
+            if miss:
+                exp_early.append(l)
+                exp_fill += [(l, e) for e in sorted(set(miss))]
+                resident[l, list(set(miss))] = True
+        assert b_b.miss.tolist() == exp_miss, t
+        assert st.early_outs == exp_early and st.filled == exp_fill, t
+        assert b_b.ctrl.tolist() == [0x7FFFFFFF, 0]
+        n_early += len(st.early_outs)
+    print(f"bounded fused decode: {n_early} early-outs over {base.tokens} tokens")
+    assert n_early > 0

@@ -31,8 +31,8 @@ struct PrefillWs {
         out = align_up(P * H * sizeof(float), 256);
         xb = align_up((size_t)T * H * 2, 256);
         hb = align_up(P * I * 2, 256);
-        // unit lists: at most (P / 64 + E) token blocks x (I / 64 gate/up + H / 128 down) row tiles
-        units = align_up(256 + 4 * (P / 64 + (size_t)E) * ((size_t)I / 64 + (size_t)H / 128), 256);
+        // unit lists: at most (P / 32 + E) token blocks x (I / 64 gate/up + H / 128 down) row tiles
+        units = align_up(256 + 4 * (P / 32 + (size_t)E) * ((size_t)I / 64 + (size_t)H / 128), 256);
         total = h + out + xb + hb + units;
     }
 };

@@ -31,16 +31,15 @@
 
 namespace rl {
 
-constexpr int kTcThreads = 256;
 constexpr int kNT = 128;         // max tokens per unit
-constexpr int kKC = 64;          // K elements per chunk
-constexpr int kStageA = 128 * kKC * 2;
-constexpr int kStageB = kNT * kKC * 2;
-constexpr int kTmemCols = 512;   // per-block accumulators x tokens fill tensor memory at most
+#ifndef RL_TC_KC
+#define RL_TC_KC 64
+#endif
+constexpr int kKC = RL_TC_KC;    // K elements per chunk
+constexpr int kKG = kKC / 8;     // 16-byte core-matrix columns (8 values) per chunk
 
-// accumulators (256-value blocks) per row of length C, and tokens per unit
+// accumulators (256-value blocks) per row of length C
 __host__ __device__ inline int tc_nblk(int C) { return C >= 256 ? C / 256 : 1; }
-__host__ __device__ inline int tc_nt(int C) { return kTmemCols / tc_nblk(C) < kNT ? kTmemCols / tc_nblk(C) : kNT; }
 constexpr int kGuRows = 64;      // gate rows (and up rows) per gate/up unit
 constexpr int kDnRowsTc = 128;   // down rows per down unit
 
@@ -143,45 +142,101 @@ __global__ void __launch_bounds__(256) tc_convert_kernel(const float *__restrict
         xb[i] = (uint16_t)TcType<T16>::bits(x[i]);
 }
 
-// ---- the grouped GEMM -------------------------------------------------------------------------
+// ---- the grouped GEMM: a warp-specialised pipeline -------------------------------------------
+// Warp roles (18 warps):
+//   0-11  producers: for every 64-wide K chunk of a unit, gather the unit's token rows of the
+//         B operand (16-bit activations) and decode the 128 x 64 A chunk from the quantized rows
+//         into one stage of a ring (canonical K-major core-matrix layout), then arrive on the
+//         stage's "full" barrier;
+//   12    MMA issuer (lane 0): per chunk, waits "full", issues the tcgen05.mma of the chunk into
+//         the unit's tensor-memory accumulators and commits to the stage's "empty" barrier;
+//         after a unit's last chunk, commits to the accumulator's "full" barrier;
+//   13    loader: stages the next unit's token list and bulk-copies its quantized rows into the
+//         other of two raw buffers;
+//   14-17 epilogue: the four TMEM lane quadrants (warp w reads lanes 32 (w % 4) ...); applies the
+//         block scales and writes h (gate/up) or the per-pair outputs (down), then releases the
+//         accumulator and the raw buffer.
+// The accumulators (one per 256-value block, nt tokens wide) are double-buffered in tensor
+// memory, so a unit's epilogue overlaps the next unit's MMAs; the raw rows are double-buffered
+// so the next unit's copy overlaps the current unit.  Every wait is bounded; a timeout sets a
+// shared abort flag and every role leaves its loop.
+constexpr int kTcProducers = 12;
+constexpr int kTcMmaWarp = 12;
+constexpr int kTcLoadWarp = 13;
+constexpr int kTcEpiWarp0 = 14;
+constexpr int kTcThreads2 = 18 * 32;
+constexpr int kTcPT = kTcProducers * 32;              // producer threads
+constexpr int kTcBMax = (kNT * kKG + kTcPT - 1) / kTcPT;  // B pieces per producer thread and chunk
+constexpr int kTcAItems = (128 * kKG + kTcPT - 1) / kTcPT;
+#ifndef RL_TC_STAGES
+#define RL_TC_STAGES 2
+#endif
+constexpr int kTcStages = RL_TC_STAGES;
+
+// tokens per unit when the accumulators are double-buffered: 2 x nblk x nt <= 512 columns
+__host__ __device__ inline int tc_nt2(int C) { return 256 / tc_nblk(C) < kNT ? 256 / tc_nblk(C) : kNT; }
+
+struct TcMeta {        // one unit, staged by the loader
+    int e, mt, nvalid, npad;
+    uint32_t p_lo;
+    uint32_t tok[kNT];
+    uint8_t k[kNT];
+};
+
 struct TcLayout {
-    size_t raw, total;   // bytes of the raw quantized rows of one unit; total shared memory
+    size_t raw, stA, stB, o_meta, o_raw, o_st, o_u, total;
     __host__ __device__ TcLayout(int MODE, int H, int I) {
-        raw = MODE == 0 ? 2 * matrix_bytes(kGuRows, H) : matrix_bytes(kDnRowsTc, I);
-        raw = align_up(raw, 128);
-        total = 1024 + kTabBytes + raw + 2 * kStageA + 2 * kStageB;
+        raw = align_up(MODE == 0 ? 2 * matrix_bytes(kGuRows, H) : matrix_bytes(kDnRowsTc, I), 128);
+        const int nt = tc_nt2(MODE == 0 ? H : I);
+        stA = 128 * kKC * 2;
+        stB = (size_t)nt * kKC * 2;
+        o_meta = 1024 + kTabBytes;
+        o_raw = align_up(o_meta + 2 * sizeof(TcMeta), 128);
+        o_st = o_raw + 2 * raw;
+        o_u = o_st + kTcStages * (stA + stB);
+        total = o_u + (MODE == 0 ? (size_t)kGuRows * nt * sizeof(float) : 0);
     }
 };
 
 // MODE 0: gate/up -> hb (16-bit h, pair order).  MODE 1: down -> outbuf (f32, (token, k) order).
 template <typename T16, int MODE>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(PrefillArgs a, TcUnits U) {
+__global__ void __launch_bounds__(kTcThreads2, 1) tc_gemm_kernel(PrefillArgs a, TcUnits U) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t *raw_bar = reinterpret_cast<uint64_t *>(smem);       // bulk copy of a unit's rows
-    uint64_t *mma_bar = raw_bar + 1;                              // [2] one per stage
-    uint64_t *done_bar = raw_bar + 3;                             // a unit's MMAs complete
-    uint64_t *fin_bar = raw_bar + 4;                              // drain before TMEM release
-    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(smem + 64);
-    uint32_t *tok_s = reinterpret_cast<uint32_t *>(smem + 128);   // [kNT] token of each pair
-    uint8_t *k_s = smem + 128 + 4 * kNT;                          // [kNT] k of each pair
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *raw_full = bars, *raw_empty = bars + 2;          // [2] each
+    uint64_t *acc_full = bars + 4, *acc_empty = bars + 6;      // [2] each
+    uint64_t *st_full = bars + 8, *st_empty = bars + 8 + kTcStages;
+    uint64_t *fin_bar = bars + 8 + 2 * kTcStages;
+    uint64_t *ex_full = fin_bar + 1, *ex_empty = fin_bar + 2;  // gate/up epilogue: u parked / consumed
+    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(smem + 256);
+    int *abort_s = reinterpret_cast<int *>(smem + 260);
     uint4 *tab = reinterpret_cast<uint4 *>(smem + 1024);
     const TcLayout lay(MODE, a.H, a.I);
-    uint8_t *raw = smem + 1024 + kTabBytes;
-    uint8_t *stA = raw + lay.raw;                                 // [2][kStageA]
-    uint8_t *stB = stA + 2 * kStageA;                             // [2][kStageB]
-    float *u_s = reinterpret_cast<float *>(stA);                  // epilogue exchange (gate/up)
+    TcMeta *meta = reinterpret_cast<TcMeta *>(smem + lay.o_meta);
+    uint8_t *rawb = smem + lay.o_raw;                            // [2][lay.raw]
+    uint8_t *stg = smem + lay.o_st;                              // [kTcStages][stA + stB]
+    float *u_s = reinterpret_cast<float *>(smem + lay.o_u);      // [kGuRows][nt] (gate/up)
 
     if (ld_ctrl(a.ctrl) <= a.layer) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int C = MODE == 0 ? a.H : a.I;  // K of this GEMM (row length)
+    const int nblk = tc_nblk(C), nt = tc_nt2(C);
+    const int nch = C / kKC;
+    const uint32_t acc_cols = (uint32_t)(nblk * nt);  // one accumulator set; two are allocated
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(&raw_bar[i], 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], (i >= 2 && i < 4) ? kTcProducers + 4 : (i >= 6 ? 4 : 1));
+        for (int i = 0; i < kTcStages; ++i) {
+            mbar_init(&st_full[i], kTcProducers);
+            mbar_init(&st_empty[i], 1);
+        }
+        mbar_init(fin_bar, 1);
+        mbar_init(ex_full, 2);   // the two up-row warps
+        mbar_init(ex_empty, 2);  // the two gate-row warps
+        *abort_s = 0;
         fence_mbar_init();
     }
-    const int C = MODE == 0 ? a.H : a.I;                 // K of this GEMM (row length)
-    const int nblk = tc_nblk(C), nt = tc_nt(C);
-    const uint32_t tcols = (uint32_t)(nblk * nt);        // 128, 256 or 512
     if (warp == 0) {
-        tc::tmem_alloc(tmem_s, tcols);
+        tc::tmem_alloc(tmem_s, 512);
         tc::tmem_relinquish();
     }
     build_pair_table_t<T16>(tab, a.codebook);
@@ -189,138 +244,214 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(PrefillArgs a, T
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_s;
-
-    const int nch = C / kKC;
-    const size_t rowb_q = matrix_bytes(1, a.H);          // bytes of an H-wide row (gate/up)
-    const size_t matb = matrix_bytes(a.I, a.H);
     const uint32_t count = __ldcg(&U.counts[MODE]);
     const uint32_t *units = MODE == 0 ? U.gu : U.dn;
-    const uint4 *tabc = tab + (lane & (kTabCopies - 1));
-    uint32_t gc = 0, nunits = 0;
+    const uint32_t nmine = count > blockIdx.x ? (count - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
+    const size_t rowb_q = matrix_bytes(1, a.H);  // bytes of an H-wide row (gate/up)
+    const size_t matb = matrix_bytes(a.I, a.H);
     bool failed = false;
+    auto wait = [&](uint64_t *bar, uint32_t parity) {  // whole warp; bounded; sets the abort flag
+        if (!mbar_spin_warp(bar, parity)) {
+            if (lane == 0) atomicExch(abort_s, 1);
+            failed = true;
+        }
+        return !failed;
+    };
+    auto aborted = [&]() { return *reinterpret_cast<volatile int *>(abort_s) != 0; };
 
-    for (uint32_t ui = blockIdx.x; ui < count; ui += gridDim.x) {
-        const uint32_t uw = __ldcg(&units[ui]);
-        const int e = uw & 1023, tb = (uw >> 10) & 1023, mt = uw >> 20;
-        const uint32_t pe0 = __ldcg(&a.offs[e]), pe1 = __ldcg(&a.offs[e + 1]);
-        const uint32_t p_lo = pe0 + tb * nt;
-        const int nvalid = (int)min((uint32_t)nt, pe1 - p_lo);
-        const int npad = (nvalid + 15) & ~15;
-        if (tid < nvalid) {
-            tok_s[tid] = __ldcg(&a.pair_tok[p_lo + tid]);
-            k_s[tid] = __ldcg(&a.pair_k[p_lo + tid]);
-        }
-        __syncthreads();
-        // the unit's expert record
-        const uint64_t slot = __ldcg(&a.slots[(size_t)tok_s[0] * a.K + k_s[0]]);
-        const bool bad = slot == 0 || (slot & 15);
-        if (bad) {
-            if (tid == 0) dev_error(a.ctrl, slot == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN);
-            __syncthreads();
-            continue;
-        }
-        const uint8_t *rec = reinterpret_cast<const uint8_t *>(slot);
-        if (tid == 0) {
-            if (MODE == 0) {
-                const uint32_t b = (uint32_t)(kGuRows * rowb_q);
-                const uint8_t *g = rec + (size_t)mt * kGuRows * rowb_q;
-                mbar_arrive_expect_tx(raw_bar, 2 * b);
-                bulk_g2s(raw, g, b, raw_bar);
-                bulk_g2s(raw + b, g + matb, b, raw_bar);
-            } else {
-                const uint32_t b = (uint32_t)matrix_bytes(kDnRowsTc, a.I);
-                mbar_arrive_expect_tx(raw_bar, b);
-                bulk_g2s(raw, rec + 2 * matb + matrix_bytes(mt * kDnRowsTc, a.I), b, raw_bar);
+    if (warp == kTcLoadWarp) {
+        // ---------------- loader ----------------
+        uint32_t issued = 0;
+        for (uint32_t k = 0; k < nmine && !failed && !aborted(); ++k) {
+            const int rb = k & 1;
+            if (k >= 2 && !wait(&raw_empty[rb], ((k >> 1) - 1) & 1)) break;
+            const uint32_t uw = __ldcg(&units[blockIdx.x + k * gridDim.x]);
+            const int e = uw & 1023, tb = (uw >> 10) & 1023, mt = uw >> 20;
+            const uint32_t pe0 = __ldcg(&a.offs[e]), pe1 = __ldcg(&a.offs[e + 1]);
+            const uint32_t p_lo = pe0 + tb * nt;
+            const int nvalid = (int)min((uint32_t)nt, pe1 - p_lo);
+            TcMeta &m = meta[rb];
+            for (int i = lane; i < nvalid; i += 32) {
+                m.tok[i] = __ldcg(&a.pair_tok[p_lo + i]);
+                m.k[i] = __ldcg(&a.pair_k[p_lo + i]);
             }
-        }
-        // B rows of chunk c go to stage (gc + c) & 1
-        auto issue_b = [&](int c, uint8_t *dstB) {
-            for (int i = tid; i < npad * 8; i += kTcThreads) {
-                const int n = i % npad, j = i / npad;
-                uint8_t *d = dstB + ((n >> 3) * 8 + j) * 128 + (n & 7) * 16;
-                if (n < nvalid) {
-                    const uint16_t *src = MODE == 0
-                                              ? a.xb16 + (size_t)tok_s[n] * a.H + c * kKC + j * 8
-                                              : a.hb16 + (size_t)(p_lo + n) * a.I + c * kKC + j * 8;
-                    tc::cp_async16(d, src);
+            if (lane == 0) {
+                m.e = e;
+                m.mt = mt;
+                m.nvalid = nvalid;
+                m.npad = (nvalid + 15) & ~15;
+                m.p_lo = p_lo;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                const uint64_t slot = __ldcg(&a.slots[(size_t)m.tok[0] * a.K + m.k[0]]);
+                if (slot == 0 || (slot & 15)) {
+                    // nothing is copied: the unit's outputs are garbage and the host sees the flag
+                    dev_error(a.ctrl, slot == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN);
+                    mbar_arrive(&raw_full[rb]);
                 } else {
-                    *reinterpret_cast<uint4 *>(d) = make_uint4(0u, 0u, 0u, 0u);
+                    const uint8_t *rec = reinterpret_cast<const uint8_t *>(slot);
+                    uint8_t *dst = rawb + rb * lay.raw;
+                    if (MODE == 0) {
+                        const uint32_t b = (uint32_t)(kGuRows * rowb_q);
+                        const uint8_t *g = rec + (size_t)mt * kGuRows * rowb_q;
+                        mbar_arrive_expect_tx(&raw_full[rb], 2 * b);
+                        bulk_g2s(dst, g, b, &raw_full[rb]);
+                        bulk_g2s(dst + b, g + matb, b, &raw_full[rb]);
+                    } else {
+                        const uint32_t b = (uint32_t)matrix_bytes(kDnRowsTc, a.I);
+                        mbar_arrive_expect_tx(&raw_full[rb], b);
+                        bulk_g2s(dst, rec + 2 * matb + matrix_bytes(mt * kDnRowsTc, a.I), b, &raw_full[rb]);
+                    }
                 }
             }
-            tc::cp_async_commit();
-        };
-        issue_b(0, stB + (gc & 1) * kStageB);
-        failed |= !mbar_wait(raw_bar, nunits & 1);
-        if ((failed = __syncthreads_or(failed) != 0)) break;
-        const uint32_t idesc = tc::instr_desc(TcType<T16>::fmt, 128, npad);
-        for (int c = 0; c < nch; ++c, ++gc) {
-            const int s = gc & 1;
-            // the other stage was last read by the MMAs of chunk gc - 1
-            if (gc >= 1) failed |= !mbar_wait(&mma_bar[(gc - 1) & 1], ((gc - 1) >> 1) & 1);
-            if (c + 1 < nch) issue_b(c + 1, stB + (s ^ 1) * kStageB);
-            // decode this thread's items of the 128 x 64 A chunk into stage s
-            uint8_t *dA = stA + s * kStageA;
-            for (int i = tid; i < 128 * 8; i += kTcThreads) {
-                const int row = i & 127, j = i >> 7;
-                int r = row;
-                const uint8_t *rb = raw;
-                if (MODE == 0 && row >= kGuRows) {  // rows 64..127: the up matrix
-                    r = row - kGuRows;
-                    rb = raw + matrix_bytes(kGuRows, a.H);
-                }
-                const int G = r * (C / 8) + c * 8 + j;  // flat group index inside the raw rows
-                const uint8_t *blk = rb + (G >> 5) * kBlockBytes;
-                const uint32_t gs = *reinterpret_cast<const uint16_t *>(blk + 2 + 2 * (G & 31));
-                const uint4 q = tabc[(gs & 0xffu) * kTabCopies];
-                const uint32_t sgn = (gs >> 8) & 0xffu;
-                const uint32_t s2 = sgn | ((sgn << 15) & 0x007f0000u);
-                uint4 v;  // +-codebook value, exact in 16 bits; the block scale is applied later
-                v.x = q.x ^ ((s2 << 15) & 0x80008000u);
-                v.y = q.y ^ ((s2 << 13) & 0x80008000u);
-                v.z = q.z ^ ((s2 << 11) & 0x80008000u);
-                v.w = q.w ^ ((s2 << 9) & 0x80008000u);
-                *reinterpret_cast<uint4 *>(dA + ((row >> 3) * 8 + j) * 128 + (row & 7) * 16) = v;
-            }
-            if (c + 1 < nch) tc::cp_async_wait<1>();
-            else tc::cp_async_wait<0>();
-            fence_proxy_async_smem();
-            if ((failed = __syncthreads_or(failed) != 0)) break;
-            if (tid == 0) {
-                tc::fence_after();
-                const uint32_t aB = tc::s_addr(dA), bB = tc::s_addr(stB + s * kStageB);
-                // chunk c lies in 256-value block c * kKC / 256 of the row: its own accumulator
-                const int blk = nblk == 1 ? 0 : (c * kKC) / 256;
-                const bool first = (c * kKC) % 256 == 0 || nblk == 1 && c == 0;
+            __syncwarp();
+            issued = k + 1;
+        }
+        // every copy this warp issued must have landed before the CTA may exit
+        for (uint32_t k = issued >= 2 ? issued - 2 : 0; k < issued; ++k) mbar_wait_warp(&raw_full[k & 1], (k >> 1) & 1);
+    } else if (warp < kTcProducers) {
+        // ---------------- producers ----------------
+        const uint4 *tabc = tab + (lane & (kTabCopies - 1));
+        uint32_t g = 0;  // chunk counter over all units
+        for (uint32_t k = 0; k < nmine && !failed; ++k) {
+            const int rb = k & 1;
+            if (!wait(&raw_full[rb], (k >> 1) & 1)) break;
+            const TcMeta &m = meta[rb];
+            const int nvalid = m.nvalid, npad = m.npad;
+            const uint8_t *raw = rawb + rb * lay.raw;
+            // B pieces of chunk c for this thread: i = tid + kTcPT * t < npad * 8
+            auto load_b = [&](int c, uint4 (&bv)[kTcBMax]) {
 #pragma unroll
-                for (int kk = 0; kk < kKC / 16; ++kk)
-                    tc::mma_f16(tmem + (uint32_t)(blk * nt), tc::smem_desc(aB + kk * 256, 128, 1024),
-                                tc::smem_desc(bB + kk * 256, 128, 1024), idesc, (first && kk == 0) ? 0u : 1u);
-                tc::commit(&mma_bar[s]);
+                for (int t = 0; t < kTcBMax; ++t) {
+                    const int i = tid + kTcPT * t;
+                    const int n = i % npad, j = i / npad;
+                    bv[t] = make_uint4(0u, 0u, 0u, 0u);
+                    if (i < npad * kKG && n < nvalid) {
+                        const uint16_t *src = MODE == 0 ? a.xb16 + (size_t)m.tok[n] * a.H + c * kKC + j * 8
+                                                        : a.hb16 + (size_t)(m.p_lo + n) * a.I + c * kKC + j * 8;
+                        bv[t] = __ldg(reinterpret_cast<const uint4 *>(src));
+                    }
+                }
+            };
+            uint4 bv[kTcBMax];
+            load_b(0, bv);
+            for (int c = 0; c < nch && !failed; ++c, ++g) {
+                const int s = g % kTcStages;
+                if (g >= (uint32_t)kTcStages && !wait(&st_empty[s], ((g / kTcStages) - 1) & 1)) break;
+                if (aborted()) { failed = true; break; }
+                uint8_t *dA = stg + s * (lay.stA + lay.stB);
+                uint8_t *dB = dA + lay.stA;
+                // B of this chunk (loaded one chunk ahead), then the loads of the next chunk
+#pragma unroll
+                for (int t = 0; t < kTcBMax; ++t) {
+                    const int i = tid + kTcPT * t;
+                    if (i < npad * kKG) {
+                        const int n = i % npad, j = i / npad;
+                        *reinterpret_cast<uint4 *>(dB + ((n >> 3) * kKG + j) * 128 + (n & 7) * 16) = bv[t];
+                    }
+                }
+                if (c + 1 < nch) load_b(c + 1, bv);
+                // A: the 128 x 64 chunk as +-codebook values (exact in 16 bits), no block scale;
+                // all loads of the thread's items first, then the stores
+                uint32_t gs[kTcAItems];
+                int row_[kTcAItems], j_[kTcAItems];
+#pragma unroll
+                for (int t = 0; t < kTcAItems; ++t) {
+                    const int i = tid + kTcPT * t;
+                    const int row = i & 127, j = i >> 7;
+                    row_[t] = row;
+                    j_[t] = j;
+                    gs[t] = 0;
+                    if (i < 128 * kKG) {
+                        int r = row;
+                        const uint8_t *rb_ = raw;
+                        if (MODE == 0 && row >= kGuRows) {  // rows 64..127: the up matrix
+                            r = row - kGuRows;
+                            rb_ = raw + matrix_bytes(kGuRows, a.H);
+                        }
+                        const int G = r * (C / 8) + c * kKG + j;  // flat group index inside the raw rows
+                        gs[t] = *reinterpret_cast<const uint16_t *>(rb_ + (G >> 5) * kBlockBytes + 2 + 2 * (G & 31));
+                    }
+                }
+                uint4 q[kTcAItems];
+#pragma unroll
+                for (int t = 0; t < kTcAItems; ++t) q[t] = tabc[(gs[t] & 0xffu) * kTabCopies];
+#pragma unroll
+                for (int t = 0; t < kTcAItems; ++t) {
+                    if (tid + kTcPT * t < 128 * kKG) {
+                        const uint32_t sgn = (gs[t] >> 8) & 0xffu;
+                        const uint32_t s2 = sgn | ((sgn << 15) & 0x007f0000u);
+                        uint4 v;
+                        v.x = q[t].x ^ ((s2 << 15) & 0x80008000u);
+                        v.y = q[t].y ^ ((s2 << 13) & 0x80008000u);
+                        v.z = q[t].z ^ ((s2 << 11) & 0x80008000u);
+                        v.w = q[t].w ^ ((s2 << 9) & 0x80008000u);
+                        const int row = row_[t];
+                        *reinterpret_cast<uint4 *>(dA + ((row >> 3) * kKG + j_[t]) * 128 + (row & 7) * 16) = v;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&st_full[s]);
+            }
+            if (failed) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[rb]);
+        }
+    } else if (warp == kTcMmaWarp) {
+        // ---------------- MMA issuer ----------------
+        uint32_t g = 0;
+        for (uint32_t k = 0; k < nmine && !failed; ++k) {
+            const int ab = k & 1;
+            if (k >= 2 && !wait(&acc_empty[ab], ((k >> 1) - 1) & 1)) break;
+            for (int c = 0; c < nch; ++c, ++g) {
+                const int s = g % kTcStages;
+                if (!wait(&st_full[s], (g / kTcStages) & 1)) break;
+                if (lane == 0) {
+                    tc::fence_after();
+                    const int npad = meta[k & 1].npad;
+                    const uint32_t idesc = tc::instr_desc(TcType<T16>::fmt, 128, npad);
+                    const uint8_t *dA = stg + s * (lay.stA + lay.stB);
+                    const uint32_t aB = tc::s_addr(dA), bB = tc::s_addr(dA + lay.stA);
+                    const int blk = nblk == 1 ? 0 : (c * kKC) / 256;
+                    const bool first = nblk == 1 ? c == 0 : (c * kKC) % 256 == 0;
+                    const uint32_t d = tmem + (uint32_t)(ab * acc_cols + blk * nt);
+#pragma unroll
+                    for (int kk = 0; kk < kKC / 16; ++kk)
+                        tc::mma_f16(d, tc::smem_desc(aB + kk * 256, 128, kKG * 128),
+                                    tc::smem_desc(bB + kk * 256, 128, kKG * 128), idesc, (first && kk == 0) ? 0u : 1u);
+                    tc::commit(&st_empty[s]);
+                    if (c == nch - 1) tc::commit(&acc_full[ab]);
+                }
+                __syncwarp();
             }
         }
-        if (failed) break;
-        if (tid == 0) tc::commit(done_bar);
-        failed |= !mbar_wait(done_bar, nunits & 1);
-        ++nunits;
-        if ((failed = __syncthreads_or(failed) != 0)) break;
-        tc::fence_after();
-        // ---- epilogue: warps 0..3 own TMEM lanes 0..127 = A rows ---------------------------------
-        // D[row][n] = sum_b d[row][b] * D_b[row][n], with D_b at TMEM columns b * nt + n
-        if (warp < 4) {
-            const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-            int r = tid;                              // row inside this unit's raw rows
-            const uint8_t *rb = raw;
-            if (MODE == 0 && tid >= kGuRows) {
-                r = tid - kGuRows;
-                rb = raw + matrix_bytes(kGuRows, a.H);
+    } else if (warp >= kTcEpiWarp0) {
+        // ---------------- epilogue ----------------
+        const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31 = A rows
+        const int row = quad * 32 + lane;
+        for (uint32_t k = 0; k < nmine && !failed; ++k) {
+            const int ab = k & 1, rb = k & 1;
+            if (!wait(&acc_full[ab], (k >> 1) & 1)) break;
+            tc::fence_after();
+            const TcMeta &m = meta[rb];
+            const int nvalid = m.nvalid, npad = m.npad, mt = m.mt;
+            const uint8_t *raw = rawb + rb * lay.raw;
+            int r = row;
+            const uint8_t *rr = raw;
+            if (MODE == 0 && row >= kGuRows) {
+                r = row - kGuRows;
+                rr = raw + matrix_bytes(kGuRows, a.H);
             }
             float dsc[8];
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 const int G = r * (C / 8) + (nblk == 1 ? 0 : 32 * b);
-                dsc[b] = b < nblk ? fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(rb + (G >> 5) * kBlockBytes))
+                dsc[b] = b < nblk ? fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(rr + (G >> 5) * kBlockBytes))
                                   : 0.f;
             }
+            const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(ab * acc_cols);
             auto scaled16 = [&](int c0, float (&acc)[16]) {
 #pragma unroll
                 for (int q = 0; q < 16; ++q) acc[q] = 0.f;
@@ -333,53 +464,62 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(PrefillArgs a, T
                 }
             };
             if (MODE == 0) {
-                if (warp >= 2) {  // up rows: park u in shared memory
+                if (row >= kGuRows) {  // up rows: park u once the gate rows have used the last one
+                    if (k >= 1 && !wait(ex_empty, (k - 1) & 1)) break;
                     for (int c0 = 0; c0 < npad; c0 += 16) {
                         float acc[16];
                         scaled16(c0, acc);
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) u_s[r * kNT + c0 + q] = acc[q];
+                        for (int q = 0; q < 16; ++q) u_s[r * nt + c0 + q] = acc[q];
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ex_full);
+                } else {               // gate rows: h = silu(g) * u
+                    if (!wait(ex_full, k & 1)) break;
+                    uint16_t *hb = a.hb16 + (size_t)m.p_lo * a.I + (size_t)mt * kGuRows + r;
+                    for (int c0 = 0; c0 < npad; c0 += 16) {
+                        float acc[16];
+                        scaled16(c0, acc);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const int n = c0 + q;
+                            if (n < nvalid) hb[(size_t)n * a.I] = (uint16_t)TcType<T16>::bits(silu(acc[q]) * u_s[r * nt + n]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ex_empty);
                 }
             } else {
-                const int orow = mt * kDnRowsTc + tid;  // output row of H
+                const int orow = mt * kDnRowsTc + row;  // output row of H
                 for (int c0 = 0; c0 < npad; c0 += 16) {
                     float acc[16];
                     scaled16(c0, acc);
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
                         const int n = c0 + q;
-                        if (n < nvalid) a.outbuf[((size_t)tok_s[n] * a.K + k_s[n]) * a.H + orow] = acc[q];
+                        if (n < nvalid) a.outbuf[((size_t)m.tok[n] * a.K + m.k[n]) * a.H + orow] = acc[q];
                     }
                 }
             }
-            if (MODE == 0) asm volatile("bar.sync 1, 128;" ::: "memory");  // up rows parked (warps 0-3 only)
-            if (MODE == 0 && warp < 2) {  // gate rows: h = silu(g) * u
-                uint16_t *hb = a.hb16 + (size_t)p_lo * a.I + (size_t)mt * kGuRows + r;
-                for (int c0 = 0; c0 < npad; c0 += 16) {
-                    float acc[16];
-                    scaled16(c0, acc);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int n = c0 + q;
-                        if (n < nvalid) hb[(size_t)n * a.I] = (uint16_t)TcType<T16>::bits(silu(acc[q]) * u_s[r * kNT + n]);
-                    }
-                }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&acc_empty[ab]);
+                mbar_arrive(&raw_empty[rb]);
             }
         }
-        tc::fence_before();
-        __syncthreads();
     }
-    if (failed && tid == 0) dev_error(a.ctrl, RL_DEVERR_WAIT_TIMEOUT);
+    if (failed && lane == 0) dev_error(a.ctrl, RL_DEVERR_WAIT_TIMEOUT);
     // drain every tcgen05 operation this CTA issued, then release tensor memory
-    if (tid == 0) {
+    __syncthreads();
+    if (tid == kTcMmaWarp * 32) {
         tc::commit(fin_bar);
         mbar_wait(fin_bar, 0);
     }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    if (warp == 0) tc::tmem_dealloc(tmem, tcols);
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 template <typename T16>
@@ -390,7 +530,7 @@ static rl_status run_tc(const PrefillArgs &a0, cudaStream_t s) {
     TcUnits U;
     uint8_t *ub = reinterpret_cast<uint8_t *>(a.units);
     U.counts = reinterpret_cast<uint32_t *>(ub);
-    const int nt_gu = tc_nt(a.H), nt_dn = tc_nt(a.I);
+    const int nt_gu = tc_nt2(a.H), nt_dn = tc_nt2(a.I);
     U.max_gu = tc_max_units(P, E, nt_gu, gu_tiles);
     U.max_dn = tc_max_units(P, E, nt_dn, dn_tiles);
     U.gu = reinterpret_cast<uint32_t *>(ub + 256);
@@ -407,7 +547,7 @@ static rl_status run_tc(const PrefillArgs &a0, cudaStream_t s) {
         const TcLayout lay(0, a.H, a.I);
         st = allow_smem((const void *)tc_gemm_kernel<T16, 0>, lay.total);
         if (st != RL_OK) return st;
-        tc_gemm_kernel<T16, 0><<<(int)std::min<size_t>(sms, U.max_gu), kTcThreads, lay.total, s>>>(a, U);
+        tc_gemm_kernel<T16, 0><<<(int)std::min<size_t>(sms, U.max_gu), kTcThreads2, lay.total, s>>>(a, U);
         st = check_launch("moe_prefill_chunk gate/up");
         if (st != RL_OK) return st;
     }
@@ -415,7 +555,7 @@ static rl_status run_tc(const PrefillArgs &a0, cudaStream_t s) {
         const TcLayout lay(1, a.H, a.I);
         st = allow_smem((const void *)tc_gemm_kernel<T16, 1>, lay.total);
         if (st != RL_OK) return st;
-        tc_gemm_kernel<T16, 1><<<(int)std::min<size_t>(sms, U.max_dn), kTcThreads, lay.total, s>>>(a, U);
+        tc_gemm_kernel<T16, 1><<<(int)std::min<size_t>(sms, U.max_dn), kTcThreads2, lay.total, s>>>(a, U);
         st = check_launch("moe_prefill_chunk down");
         if (st != RL_OK) return st;
     }

@@ -118,6 +118,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// Non-blocking probe of phase `parity` (mbarrier.test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+constexpr uint32_t kSpinPolls = 1u << 26;  // test_wait polls (tens of cycles each): about a second
+// Bounded spin on test_wait by lane 0 of the warp (the other lanes park in __syncwarp): for
+// the hand-offs of a pipeline, where the wake-up delay of a suspended try_wait is too long.
+// Call with the whole warp; the result is warp-uniform.
+__device__ __forceinline__ bool mbar_spin_warp(uint64_t *bar, uint32_t parity) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) {
+        for (uint32_t i = 0; i < kSpinPolls; ++i)
+            if (mbar_test_wait(bar, parity)) {
+                ok = 1;
+                break;
+            }
+    }
+    return __shfl_sync(kFull, ok, 0) != 0;
+}
 // The same wait made by lane 0 of the warp alone while the other lanes park in __syncwarp, so
 // that a waiting warp does not keep the shared-memory pipe busy with polls (which slows the
 // warps that compute).  Call with the whole warp; the result is warp-uniform.

@@ -131,6 +131,27 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def token_shard(rank: int, T: int) -> tuple[int, int]:
+    """Weak scaling with no exchange: rank r runs its own T tokens, numbers r*T .. r*T+T-1 of
+    the workload's seeded token stream, so the ranks' shards are disjoint."""
+    return rank * T, T
+
+
+def reduce_max(v: float, dev, ws: int) -> float:
+    """The maximum of v over the ranks (the job time is the slowest rank's)."""
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(ws: int, T: int, steps: int, ms_max: float) -> float:
+    """Whole-job tokens/s: the tokens of every rank over the slowest rank's time."""
+    return ws * T * steps / (ms_max / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -253,7 +274,8 @@ def run_ours(a):
     model = engine.Model(w, device=dev, layers=a.layers)
     b = engine.DecodeBuffers.make(model)
     # this rank's tokens (weak scaling: every rank decodes its own 256 / 1000 tokens)
-    x_host = torch.from_numpy(synth.tokens(w, rank * T, T)).pin_memory()
+    t0, _ = token_shard(rank, T)
+    x_host = torch.from_numpy(synth.tokens(w, t0, T)).pin_memory()
     x_in = x_host.to(dev)
     y_out = torch.zeros_like(x_in)
     y_host = torch.empty_like(x_host).pin_memory()
@@ -306,11 +328,8 @@ def run_ours(a):
     ms = ev0.elapsed_time(ev1)
     ctrl = b.ctrl.cpu().tolist()
     assert ctrl[0] == L.RL_NO_EARLY_OUT and ctrl[1] == 0, f"device control block {ctrl}"
-    t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    ms_max = float(t_max.item())
-    value = ws * T * a.steps / (ms_max / 1e3)
+    ms_max = reduce_max(ms, dev, ws)
+    value = weak_value(ws, T, a.steps, ms_max)
 
     # ---- end to end: pinned host x -> device, the tokens, device -> pinned host y ----
     h2d = x_host.numel() * 4
@@ -325,10 +344,7 @@ def run_ours(a):
             y_host.copy_(y_out, non_blocking=True)
         e1.record(stream)
     barrier()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_value = ws * T * a.steps / (float(e2e_ms.item()) / 1e3)
+    e2e_value = weak_value(ws, T, a.steps, reduce_max(e0.elapsed_time(e1), dev, ws))
 
     peak, peak_kind = _peaks()
     per_layer_bytes = w.top_k * w.record_bytes + w.n_experts * w.hidden * 4 + 2 * w.hidden * 4

@@ -72,3 +72,29 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     assert st == RL_ERR_INVALID
     st = lib.rl_rmsnorm(fake, fake, 4, 2048, -1.0, None)
     assert st == RL_ERR_INVALID
+
+
+def test_decode_stack_host_checks(lib):
+    """moe_decode_stack: workspace query and the checks made before any launch."""
+    from quantized_moe_expert_rl_gb300._lib import RL_ERR_INVALID, RL_OK, RlShape
+    s = RlShape.of(2048, 512, 10, 512, 48)
+    need = lib.moe_decode_stack_workspace_bytes(ctypes.byref(s))
+    assert need >= 256 + 512 * 4 + 10 * 512 * 4
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake, -1.0, fake, None, fake, fake, fake, fake, fake, fake, fake, None, None, fake]
+    # layers outside [0, n_layers)
+    assert lib.moe_decode_stack(ctypes.byref(s), 40, 9, *args, need, None) == RL_ERR_INVALID
+    assert b"layers" in lib.rl_last_error()
+    # workspace too small
+    assert lib.moe_decode_stack(ctypes.byref(s), 0, 48, *args, need - 256, None) == RL_ERR_INVALID
+    assert b"workspace" in lib.rl_last_error()
+    # NULL required buffer (x)
+    bad = list(args)
+    bad[0] = None
+    assert lib.moe_decode_stack(ctypes.byref(s), 0, 48, *bad, need, None) == RL_ERR_INVALID
+    # misaligned router weights
+    bad = list(args)
+    bad[2] = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.moe_decode_stack(ctypes.byref(s), 0, 48, *bad, need, None) == RL_ERR_INVALID
+    # zero layers: nothing to do, no launch
+    assert lib.moe_decode_stack(ctypes.byref(s), 48, 0, *args, need, None) == RL_OK

@@ -285,7 +285,7 @@ def run_ours(a):
     if fused:
         # one moe_decode_stack launch per token runs all layers (plus the copy of x into y)
         def token(t):
-            engine.enqueue_decode_token_fused(model, b, x_in[t], y_out[t])
+            engine.enqueue_decode_token_fused(model, b, x_in[t], y_out[t], pregate=a.pregate)
         launches_per_token = 1
 
         def step():
@@ -362,7 +362,7 @@ def run_ours(a):
                     s_.record(stream)
                     L.moe_decode_stack(model.shape, 0, model.L, ybuf, engine.EPS, model.routers, model.bias,
                                        model.table, model.codebook, b.ids, b.weights, b.slots, b.miss, b.ctrl,
-                                       None, None, b.stack_ws, b.stack_ws.numel(), stream)
+                                       None, None, a.pregate, None, b.stack_ws, b.stack_ws.numel(), stream)
                     e_.record(stream)
         stream.synchronize()
         durs = np.array([s_.elapsed_time(e_) for s_, e_ in evs]) * 1e-3
@@ -551,6 +551,9 @@ def main():
     ap.add_argument("--decode-path", choices=["fused", "chain"], default="fused",
                     help="stacked decode: one moe_decode_stack launch per token, or per-token graphs of the "
                          "per-layer rl_route + moe_decode chain")
+    ap.add_argument("--pregate", type=int, default=0,
+                    help="fused decode: experts of the next layer prefetched into L2 on the pre-gated "
+                         "prediction (0 = off)")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers of the stacked workload (profiling of smaller cases)")
     a = ap.parse_args()

@@ -190,6 +190,13 @@ rl_status moe_decode_static(const rl_moe_shape *shp, int32_t layer, const float 
  * [n_layers][K] (rows of the run are written); miss uint32 [n_layers] (accumulated);
  * logits_out f32 [n_layers][E] or NULL; x_hist f32 [n_layers][H] or NULL (x_l, the input of
  * each layer run, for validation).  Does nothing when ctrl[0] < layer0.
+ * pregate (0 <= pregate <= min(32, E)): pre-gated expert prefetch ("Red Lite dev23 - per-layer
+ * early-out and pre-gated expert prefetch", "What changed"): during layer l the next layer's
+ * router is applied to layer l's normalised input, and the records of its `pregate` highest-
+ * scoring resident experts are prefetched from HBM into L2, so that layer l + 1's expert copies
+ * hit L2 when the prediction is right.  0 turns it off.  It never changes a result.
+ * pregate_hits uint32 [n_layers] or NULL: for every layer after the first of the run, how
+ * many of its K selected experts were in the previous layer's prediction.
  * ws: moe_decode_stack_workspace_bytes(shp) bytes, 16-byte aligned, zero-filled before its
  * first use; it holds a grid-barrier counter that grows across calls, so calls sharing one
  * workspace must not overlap on the GPU, and after a call that raised RL_DEVERR_WAIT_TIMEOUT
@@ -201,8 +208,8 @@ size_t moe_decode_stack_workspace_bytes(const rl_moe_shape *shp);
 rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x, float norm_eps,
                            const float *w_router, const float *bias, const uint64_t *residency,
                            const int8_t *codebook, int32_t *ids, float *weights, uint64_t *slots,
-                           uint32_t *miss, int32_t *ctrl, float *logits_out, float *x_hist, void *ws,
-                           size_t ws_bytes, void *stream);
+                           uint32_t *miss, int32_t *ctrl, float *logits_out, float *x_hist, int32_t pregate,
+                           uint32_t *pregate_hits, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * rl_build_pairs - (expert, token) pairs sorted by expert, stable in (t, k) order

@@ -66,7 +66,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_decode": (i32, [shp, i32, vp, f32, vp, vp, vp, vp, i32, vp, vp, sz, vp]),
         "moe_decode_static": (i32, [shp, i32, vp, f32, vp, vp, vp, vp, i32, vp, vp]),
         "moe_decode_stack_workspace_bytes": (sz, [shp]),
-        "moe_decode_stack": (i32, [shp, i32, i32, vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "moe_decode_stack": (i32, [shp, i32, i32, vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, sz,
+                                   vp]),
         "rl_build_pairs_workspace_bytes": (sz, [shp, i32]),
         "rl_build_pairs": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_prefill_workspace_bytes": (sz, [shp, i32]),
@@ -154,11 +155,11 @@ def moe_decode_stack_workspace_bytes(shape) -> int:
 
 
 def moe_decode_stack(shape, layer0, n_layers, x, norm_eps, w_router, bias, residency, codebook, ids, weights, slots,
-                     miss, ctrl, logits_out, x_hist, ws, ws_bytes, stream=None):
+                     miss, ctrl, logits_out, x_hist, pregate, pregate_hits, ws, ws_bytes, stream=None):
     _check("moe_decode_stack", load().moe_decode_stack(
         ctypes.byref(shape), layer0, n_layers, ptr(x), float(norm_eps), ptr(w_router), ptr(bias), ptr(residency),
         ptr(codebook), ptr(ids), ptr(weights), ptr(slots), ptr(miss), ptr(ctrl), ptr(logits_out), ptr(x_hist),
-        ptr(ws), ws_bytes, _stream(stream)))
+        int(pregate), ptr(pregate_hits), ptr(ws), ws_bytes, _stream(stream)))
 
 
 def rl_build_pairs_workspace_bytes(shape, T) -> int:

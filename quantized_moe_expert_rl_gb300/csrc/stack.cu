@@ -41,10 +41,12 @@ namespace rl {
 constexpr int kStThreads = 512;
 constexpr int kStWarps = kStThreads / 32;
 constexpr int kStGuChunks = 2;
-constexpr int kStBars = 2 + 2 * kStGuChunks;  // [0] router rows, [1] down rows, [2..] gate/up chunks
+constexpr int kStBars = 3 + 2 * kStGuChunks;  // [0,1] router rows, [2] down rows, [3..] gate/up chunks
 constexpr uint32_t kSpinCap = 1u << 22;       // global-memory polls (~1 us each): seconds
 constexpr int kStSelWarps = 16;               // selection warps: E <= 32 * 16
-constexpr int kStHdr = 4608;                  // barriers, scalars, CTA constants, selection scratch
+constexpr int kStHdr = 4736;                  // barriers, scalars, CTA constants, selection scratch
+constexpr int kStPredMax = 32;                // experts prefetched on the pre-gated prediction
+constexpr int kStCand = 16;                   // single-warp selection: candidates per lane (E <= 512)
 // The warp that issues every bulk copy.  A memory fence waits for the bulk copies its own
 // thread has in flight, so the thread that runs the grid barrier (thread 0) never issues one.
 constexpr int kStProducer = kStWarps - 1;
@@ -54,7 +56,7 @@ __host__ __device__ inline int dn_unit(int I) { return I >= 2048 ? 1 : 2048 / I;
 
 struct StLayout {
     int rt_max, rmax, dmax, rowb, dtileb;
-    size_t o_x, o_rt, o_part, o_gu, o_dn, o_o, total;
+    size_t o_x, o_rt, o_part, o_gu, o_dn, o_o, o_h, total;
     __host__ __device__ StLayout(int H, int E, int K, int I, int G) {
         rt_max = (E + G - 1) / G;
         const int U = gu_unit(H), units = K * I / U;
@@ -65,11 +67,12 @@ struct StLayout {
         dtileb = (int)align_up(matrix_bytes(dmax, I), 16);
         o_x = kStHdr + kTabBytes;
         o_rt = o_x + (size_t)H * sizeof(float);
-        o_part = o_rt + (size_t)rt_max * H * sizeof(float);
+        o_part = o_rt + 2 * (size_t)rt_max * H * sizeof(float);  // two layers' router rows
         o_gu = o_part + align_up((size_t)rmax * 4 * sizeof(float), 16);
         o_dn = o_gu + 2 * (size_t)rmax * rowb;
         o_o = o_dn + (size_t)K * dtileb;
-        total = o_o + (size_t)K * dmax * sizeof(float);
+        o_h = o_o + align_up((size_t)K * dmax * sizeof(float), 16);
+        total = o_h + (size_t)K * I * sizeof(float);  // h of every expert, staged for the down rows
     }
 };
 
@@ -80,7 +83,8 @@ struct StCta {
     int p0, p1, ka, kb, n0, n1;  // gate/up (expert, row) pairs: two segments (experts ka, kb)
     int q0, nq;              // down output rows
     int rowb, dtileb, dmax;
-    uint32_t o_x, o_rt, o_part, o_gu, o_dn, o_o;
+    uint32_t o_x, o_rt, o_part, o_gu, o_dn, o_o, o_h;
+    uint32_t rtb;            // bytes of one router buffer
 };
 
 struct StackArgs {
@@ -98,9 +102,11 @@ struct StackArgs {
     float *logits_out;  // [L][E] or NULL
     float *x_hist;      // [L][H] or NULL
     unsigned long long *ctr;
-    float *lg;  // [E]
-    float *h;   // [K][I]
-    int layer0, nl, H, E, K, I;
+    float *lg;   // [E]
+    float *lgp;  // [E] pre-gate logits: the next layer's router on this layer's input
+    float *h;    // [K][I]
+    uint32_t *pg_hits;  // [L] or NULL
+    int layer0, nl, H, E, K, I, pregate;
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
@@ -144,7 +150,7 @@ template <int NV, int GPL, int SPLIT, int DGPL, int LPR>
 __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *bar_rt = bars, *bar_dn = bars + 1, *bar_gu = bars + 2;
+    uint64_t *bar_rt = bars, *bar_dn = bars + 2, *bar_gu = bars + 3;  // bar_rt[2]: one per router buffer
     float *scale_s = reinterpret_cast<float *>(smem + 64);
     int *stop_s = reinterpret_cast<int *>(smem + 68);
     int *ok_s = reinterpret_cast<int *>(smem + 72);
@@ -154,6 +160,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
     uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem + 512);
     int *cand_id = reinterpret_cast<int *>(smem + 1536);
     uint64_t *cand_slot = reinterpret_cast<uint64_t *>(smem + 2560);
+    int *pred_s = reinterpret_cast<int *>(smem + 4608);  // [kStPredMax] predicted ids of the next layer
     uint4 *tab = reinterpret_cast<uint4 *>(smem + kStHdr);
     constexpr int H = NV * 128;
     constexpr int U = H >= 2048 ? 1 : 2048 / H;  // gu_unit(H)
@@ -179,7 +186,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
         C.dtileb = lay.dtileb;
         C.dmax = lay.dmax;
         C.o_x = (uint32_t)lay.o_x; C.o_rt = (uint32_t)lay.o_rt; C.o_part = (uint32_t)lay.o_part;
-        C.o_gu = (uint32_t)lay.o_gu; C.o_dn = (uint32_t)lay.o_dn; C.o_o = (uint32_t)lay.o_o;
+        C.o_gu = (uint32_t)lay.o_gu; C.o_dn = (uint32_t)lay.o_dn; C.o_o = (uint32_t)lay.o_o; C.o_h = (uint32_t)lay.o_h;
+        C.rtb = (uint32_t)((size_t)lay.rt_max * H * sizeof(float));
         for (int i = 0; i < kStBars; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
     }
@@ -187,18 +195,25 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
     const int flag0 = ld_ctrl(a.ctrl);
     if (flag0 < a.layer0) return;  // an earlier layer already stopped the chain
 
-    // one thread: this CTA's router rows of layer l into shared memory
-    auto issue_router = [&](int l) {
+    // one thread: this CTA's router rows of layer index i (layer0 + i) into buffer i & 1.  The
+    // rows of layer i + 1 are in shared memory during layer i (they feed the pre-gate logits
+    // and then layer i + 1 itself); buffer b's n-th load completes phase n of bar_rt[b].
+    auto issue_router = [&](int i) {
         const uint32_t bytes = (uint32_t)((size_t)C.nr * H * sizeof(float));
-        mbar_arrive_expect_tx(bar_rt, bytes);
-        bulk_g2s(smem + C.o_rt, a.W + ((size_t)l * a.E + C.e0) * H, bytes, bar_rt);
+        mbar_arrive_expect_tx(&bar_rt[i & 1], bytes);
+        bulk_g2s(smem + C.o_rt + (i & 1) * C.rtb, a.W + ((size_t)(a.layer0 + i) * a.E + C.e0) * H, bytes,
+                 &bar_rt[i & 1]);
     };
-    if (threadIdx.x == kStProducer * 32 && C.nr > 0) issue_router(a.layer0);
+    const bool pregate = a.pregate > 0;
+    if (threadIdx.x == kStProducer * 32 && C.nr > 0) {
+        issue_router(0);
+        if (a.nl > 1) issue_router(1);
+    }
 
     unsigned long long target = 0;  // grid barrier state (thread 0)
-    // copies in flight, for the exit path: parity of the router copy (-1: none) and whether
-    // this layer's expert copies were issued
-    int rt_par = C.nr > 0 ? 0 : -1;
+    // copies in flight, for the exit path: the layer index of the last router load of each
+    // buffer (-1: none) and whether this layer's expert copies were issued
+    int rt_last[2] = {C.nr > 0 ? 0 : -1, (C.nr > 0 && a.nl > 1) ? 1 : -1};
     bool ex_issued = false;
     bool failed = false;
     uint32_t ph = 0;
@@ -219,36 +234,46 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
             if (a.x_hist && blockIdx.x == 0)
                 for (int j = threadIdx.x; j < H; j += kStThreads) a.x_hist[(size_t)l * H + j] = x_s[j];
             const int nr = C.nr;
-            if (warp < nr && !mbar_wait_warp(bar_rt, ph)) failed = true;
+            const bool pg = pregate && !last;
+            if (warp < nr && !mbar_wait_warp(&bar_rt[i & 1], (i >> 1) & 1)) failed = true;
+            if (pg && warp < nr && !mbar_wait_warp(&bar_rt[(i + 1) & 1], ((i + 1) >> 1) & 1)) failed = true;
             __syncthreads();
             if (warp < nr && !failed) {
                 const float4 *xr = reinterpret_cast<const float4 *>(x_s);
-                const float4 *wr = reinterpret_cast<const float4 *>(smem + C.o_rt) + (size_t)warp * (H / 4);
                 const bool norm = a.eps >= 0.f;
                 const float r = *scale_s;
-                unsigned long long a0 = 0, a1 = 0;
+                // this layer's logit of row e0 + warp, then (pre-gating) the next layer's
+#pragma unroll 1
+                for (int q = 0; q < (pg ? 2 : 1); ++q) {
+                    const float4 *wr = reinterpret_cast<const float4 *>(smem + C.o_rt + ((i + q) & 1) * C.rtb) +
+                                       (size_t)warp * (H / 4);
+                    unsigned long long a0 = 0, a1 = 0;
 #pragma unroll
-                for (int j = 0; j < NV; ++j) {
-                    float4 v = xr[lane + 32 * j];
-                    if (norm) { v.x *= r; v.y *= r; v.z *= r; v.w *= r; }
-                    const float4 w = wr[lane + 32 * j];
-                    a0 = ffma2(pack2(__float_as_uint(w.x), __float_as_uint(w.y)),
-                               pack2(__float_as_uint(v.x), __float_as_uint(v.y)), a0);
-                    a1 = ffma2(pack2(__float_as_uint(w.z), __float_as_uint(w.w)),
-                               pack2(__float_as_uint(v.z), __float_as_uint(v.w)), a1);
-                }
-                const float s = warp_sum(hsum2(a0) + hsum2(a1));
-                if (lane == 0) {
-                    const int e = C.e0 + warp;
-                    const float lv = s + (a.bias ? a.bias[(size_t)l * a.E + e] : 0.f);
-                    __stcg(a.lg + e, lv);
-                    if (a.logits_out) a.logits_out[(size_t)l * a.E + e] = lv;
+                    for (int j = 0; j < NV; ++j) {
+                        float4 v = xr[lane + 32 * j];
+                        if (norm) { v.x *= r; v.y *= r; v.z *= r; v.w *= r; }
+                        const float4 w = wr[lane + 32 * j];
+                        a0 = ffma2(pack2(__float_as_uint(w.x), __float_as_uint(w.y)),
+                                   pack2(__float_as_uint(v.x), __float_as_uint(v.y)), a0);
+                        a1 = ffma2(pack2(__float_as_uint(w.z), __float_as_uint(w.w)),
+                                   pack2(__float_as_uint(v.z), __float_as_uint(v.w)), a1);
+                    }
+                    const float s = warp_sum(hsum2(a0) + hsum2(a1));
+                    if (lane == 0) {
+                        const int e = C.e0 + warp;
+                        const float lv = s + (a.bias ? a.bias[(size_t)(l + q) * a.E + e] : 0.f);
+                        if (q == 0) {
+                            __stcg(a.lg + e, lv);
+                            if (a.logits_out) a.logits_out[(size_t)l * a.E + e] = lv;
+                        } else {
+                            __stcg(a.lgp + e, lv);
+                        }
+                    }
                 }
             }
         }
         failed = __syncthreads_or(failed) != 0;
         if (failed) break;
-        rt_par = -1;
         if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
 
         // ---------------- B: selection (the same in every CTA), expert copies ----------------
@@ -266,6 +291,13 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
                 if (lane < K) {
                     slots_s[lane] = slot;
                     w_s[lane] = w;
+                }
+                if (blockIdx.x == 0 && a.pg_hits && pregate && i > 0) {
+                    // how many of this layer's experts the previous layer predicted
+                    bool hit = false;
+                    for (int j = 0; j < a.pregate; ++j) hit |= lane < K && pred_s[j] == my_id;
+                    const int nhit = __popc(__ballot_sync(kFull, hit));
+                    if (lane == 0) a.pg_hits[l] = (uint32_t)nhit;
                 }
                 if (blockIdx.x == 0) {
                     if (lane < K) {
@@ -386,42 +418,84 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
             const float *part = reinterpret_cast<const float *>(smem + C.o_part);
             for (int t = threadIdx.x; t < np; t += kStThreads) __stcg(a.h + p0 + t, swiglu_part<SPLIT>(part + 4 * t));
         }
-        // the router rows of the next layer (every warp is done with this layer's)
-        if (C.nr > 0 && !last) {
+        // buffer i & 1 (free since phase A) takes the rows of layer i + 2; issued after this
+        // layer's expert copies so that it never delays them
+        if (C.nr > 0 && i + 2 < a.nl) {
             if (threadIdx.x == kStProducer * 32) {
                 fence_proxy_async_smem();
-                issue_router(l + 1);
+                issue_router(i + 2);
             }
-            rt_par = (int)(ph ^ 1u);
+            rt_last[i & 1] = i + 2;
         }
         if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
 
         // ---------------- D: down rows of every expert, ordered combine, residual ----------------
+        // The producer warp (idle in D when K > 8) meanwhile selects the pre-gated prediction of
+        // the next layer's experts and prefetches this CTA's slice of their records into L2
+        // ("Red Lite dev23", "What changed": pre-gated expert prefetch).
+        if (pregate && !last && warp == kStProducer) {
+            const int P = a.pregate;
+            int pid;
+            float pval;
+            warp_topk<kStCand>(a.lgp, a.E, P, pid, pval);
+            uint64_t pslot = 0;
+            if (lane < P) {
+                pred_s[lane] = pid;
+                pslot = __ldcg(a.table + (size_t)(l + 1) * a.E + pid);
+            }
+            const size_t rec = 3 * matrix_bytes(a.I, H);
+            const size_t total = (size_t)P * rec;
+            const size_t S = align_up((total + gridDim.x - 1) / gridDim.x, 16);
+            const size_t lo = (size_t)blockIdx.x * S, hi = lo + S < total ? lo + S : total;
+            if (lane < P && pslot != 0 && (pslot & 15) == 0) {
+                const size_t r0 = (size_t)lane * rec, r1 = r0 + rec;
+                const size_t b0 = lo > r0 ? lo : r0, b1 = hi < r1 ? hi : r1;
+                if (b1 > b0) prefetch_l2_bulk(reinterpret_cast<const uint8_t *>(pslot) + (b0 - r0), (uint32_t)(b1 - b0));
+            }
+            __syncwarp();
+        }
         {
+            // every group of LPR lanes owns one expert (group g: expert g % K) and every
+            // (K)-th of its rows; a warp runs as many passes as its busier half needs, so the
+            // shuffles of a row's reduction always see the whole warp
             const int nq = C.nq, K = a.K;
+            // h of all K experts into shared memory, once per CTA, lane-transposed: the q-th
+            // float4 of lane sl of a row group sits at [k][q][sl], so a group's loads do not
+            // collide on banks
+            {
+                const int I = a.I, f4 = I / 4;
+                float4 *h_s = reinterpret_cast<float4 *>(smem + C.o_h);
+                for (int f = threadIdx.x; f < K * f4; f += kStThreads) {
+                    const int k = f / f4, r = f % f4, sl = r / (2 * DGPL), q = r % (2 * DGPL);
+                    h_s[k * f4 + q * LPR + sl] = __ldcg(reinterpret_cast<const float4 *>(a.h) + f);
+                }
+                __syncthreads();
+            }
             if (nq > 0) {
-                const int wpe = kStWarps / K;  // warps per expert
-                constexpr int kRpp = 32 / LPR;   // rows per warp pass
-                const int k = warp / wpe, j = warp % wpe, sub = lane / LPR, sl = lane % LPR;
-                if (k < K) {
-                    const int I = a.I, dmax = C.dmax;
-                    float hv[8 * DGPL];
+                constexpr int kNG = kStThreads / LPR;  // lane groups in the CTA
+                const int g = threadIdx.x / LPR, sl = lane % LPR;
+                const int k = g % K, jg = g / K, ngk = (kNG - k + K - 1) / K;
+                const int mine = jg < nq ? (nq - jg + ngk - 1) / ngk : 0;
+                const int trips = (int)__reduce_max_sync(kFull, (unsigned)mine);
+                const int I = a.I, dmax = C.dmax;
+                float hv[8 * DGPL];
+                const float4 *h_s = reinterpret_cast<const float4 *>(smem + C.o_h) + (size_t)k * (I / 4);
 #pragma unroll
-                    for (int q = 0; q < 2 * DGPL; ++q) {
-                        const float4 v =
-                            __ldcg(reinterpret_cast<const float4 *>(a.h + (size_t)k * I + sl * 8 * DGPL) + q);
-                        hv[4 * q] = v.x; hv[4 * q + 1] = v.y; hv[4 * q + 2] = v.z; hv[4 * q + 3] = v.w;
-                    }
-                    if (!mbar_wait_warp(bar_dn, ph)) {
-                        failed = true;
-                    } else {
-                        const uint4 *tabc = tab + (lane & (kTabCopies - 1));
-                        const uint8_t *tile = smem + C.o_dn + (size_t)k * C.dtileb;
-                        float *o_s = reinterpret_cast<float *>(smem + C.o_o);
-                        for (int rr = j * kRpp + sub; rr < nq; rr += wpe * kRpp) {
-                            const float o = down_row<DGPL, LPR>(tile, rr, I, sl, hv, tabc);
-                            if (sl == 0) o_s[k * dmax + rr] = o;
-                        }
+                for (int q = 0; q < 2 * DGPL; ++q) {
+                    const float4 v = h_s[q * LPR + sl];
+                    hv[4 * q] = v.x; hv[4 * q + 1] = v.y; hv[4 * q + 2] = v.z; hv[4 * q + 3] = v.w;
+                }
+                if (trips > 0 && !mbar_wait_warp(bar_dn, ph)) {
+                    failed = true;
+                } else {
+                    const uint4 *tabc = tab + (lane & (kTabCopies - 1));
+                    const uint8_t *tile = smem + C.o_dn + (size_t)k * C.dtileb;
+                    float *o_s = reinterpret_cast<float *>(smem + C.o_o);
+                    for (int t = 0; t < trips; ++t) {
+                        const int rr = jg + t * ngk;
+                        const bool real = rr < nq;
+                        const float o = down_row<DGPL, LPR>(tile, real ? rr : 0, I, sl, hv, tabc);
+                        if (real && sl == 0) o_s[k * dmax + rr] = o;
                     }
                 }
             }
@@ -440,7 +514,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
     }
     // ---- exit: no copy into this CTA's shared memory may still be in flight ----
     if (threadIdx.x == 0) {
-        if (rt_par >= 0) mbar_wait(bar_rt, (uint32_t)rt_par);
+        for (int b = 0; b < 2; ++b)
+            if (rt_last[b] >= 0) mbar_wait(&bar_rt[b], (uint32_t)((rt_last[b] >> 1) & 1));
         if (ex_issued) {
             if (C.nq > 0) mbar_wait(bar_dn, ph);
             for (int bi = 0; bi < 2 * kStGuChunks; ++bi) {
@@ -499,7 +574,7 @@ using namespace rl;
 
 extern "C" size_t moe_decode_stack_workspace_bytes(const rl_moe_shape *shp) {
     if (!shp || shp->n_experts <= 0 || shp->top_k <= 0 || shp->inter <= 0) return 0;
-    return 256 + align_up((size_t)shp->n_experts * sizeof(float), 256) +
+    return 256 + 2 * align_up((size_t)shp->n_experts * sizeof(float), 256) +
            align_up((size_t)shp->top_k * shp->inter * sizeof(float), 256);
 }
 
@@ -507,7 +582,8 @@ extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, i
                                       float norm_eps, const float *w_router, const float *bias,
                                       const uint64_t *residency, const int8_t *codebook, int32_t *ids,
                                       float *weights, uint64_t *slots, uint32_t *miss, int32_t *ctrl,
-                                      float *logits_out, float *x_hist, void *ws, size_t ws_bytes, void *stream) {
+                                      float *logits_out, float *x_hist, int32_t pregate, uint32_t *pregate_hits,
+                                      void *ws, size_t ws_bytes, void *stream) {
     rl_status st = check_shape(shp);
     if (st != RL_OK) return st;
     if (layer0 < 0 || n_layers < 0 || layer0 + n_layers > shp->n_layers)
@@ -521,6 +597,8 @@ extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, i
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router) | reinterpret_cast<uintptr_t>(ws) |
          reinterpret_cast<uintptr_t>(x_hist)) & 15)
         return fail(RL_ERR_INVALID, "moe_decode_stack: x, w_router, x_hist and ws must be 16-byte aligned");
+    if (pregate < 0 || pregate > kStPredMax || pregate > shp->n_experts)
+        return fail(RL_ERR_INVALID, "moe_decode_stack: pregate %d outside [0, min(%d, n_experts)]", pregate, kStPredMax);
     if (n_layers == 0) return RL_OK;
     StackArgs a;
     a.x = x;
@@ -538,8 +616,12 @@ extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, i
     a.x_hist = x_hist;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     a.ctr = reinterpret_cast<unsigned long long *>(w8);
+    const size_t lgb = align_up((size_t)shp->n_experts * sizeof(float), 256);
     a.lg = reinterpret_cast<float *>(w8 + 256);
-    a.h = reinterpret_cast<float *>(w8 + 256 + align_up((size_t)shp->n_experts * sizeof(float), 256));
+    a.lgp = reinterpret_cast<float *>(w8 + 256 + lgb);
+    a.h = reinterpret_cast<float *>(w8 + 256 + 2 * lgb);
+    a.pg_hits = pregate_hits;
+    a.pregate = pregate;
     a.layer0 = layer0;
     a.nl = n_layers;
     a.H = shp->hidden;

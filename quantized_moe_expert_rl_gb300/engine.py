@@ -193,14 +193,17 @@ def enqueue_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_o
 
 def enqueue_decode_token_fused(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
                                keep_logits: bool = False, x_hist: torch.Tensor | None = None,
-                               layer0: int = 0) -> None:
+                               layer0: int = 0, pregate: int = 0,
+                               pregate_hits: torch.Tensor | None = None) -> None:
     """Stacked decode of one token, layers [layer0, L), in ONE launch (moe_decode_stack):
     y_out = x_in, then per layer y_out += MoE(RMSNorm(y_out)).  Bit-identical to
-    enqueue_decode_token(stacked=True).  x_hist[l] (optional) receives layer l's input."""
+    enqueue_decode_token(stacked=True).  x_hist[l] (optional) receives layer l's input.
+    pregate > 0 prefetches into L2 the next layer's predicted experts (never changes results);
+    pregate_hits[l] (optional) receives how many of layer l's experts were predicted."""
     y_out.copy_(x_in)
     L.moe_decode_stack(model.shape, layer0, model.L - layer0, y_out, EPS, model.routers, model.bias, model.table,
                        model.codebook, b.ids, b.weights, b.slots, b.miss, b.ctrl, b.logits if keep_logits else None,
-                       x_hist, b.stack_ws, b.stack_ws.numel())
+                       x_hist, pregate, pregate_hits, b.stack_ws, b.stack_ws.numel())
 
 
 @dataclass
@@ -212,7 +215,7 @@ class DecodeStats:
 
 
 def run_bounded_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
-                             x_hist: torch.Tensor | None = None) -> DecodeStats:
+                             x_hist: torch.Tensor | None = None, pregate: int = 0) -> DecodeStats:
     """One token through every layer with bounded residency ("Red Lite dev23", "What changed",
     item 1): the fused stack runs until a layer f selects an absent expert and stops there
     with y_out = x_f; the host reads the flag once, fills layer f's missing experts, re-resolves
@@ -225,8 +228,8 @@ def run_bounded_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor,
     l0 = 0
     while l0 < model.L:
         L.moe_decode_stack(shp, l0, model.L - l0, y_out, EPS, model.routers, model.bias, model.table,
-                           model.codebook, b.ids, b.weights, b.slots, b.miss, b.ctrl, None, x_hist, b.stack_ws,
-                           b.stack_ws.numel())
+                           model.codebook, b.ids, b.weights, b.slots, b.miss, b.ctrl, None, x_hist, pregate, None,
+                           b.stack_ws, b.stack_ws.numel())
         ctrl = b.ctrl.tolist()
         st.syncs += 1
         if ctrl[1] != 0:

@@ -81,7 +81,7 @@ def test_decode_stack_host_checks(lib):
     need = lib.moe_decode_stack_workspace_bytes(ctypes.byref(s))
     assert need >= 256 + 512 * 4 + 10 * 512 * 4
     fake = ctypes.c_void_p(1 << 20)
-    args = [fake, -1.0, fake, None, fake, fake, fake, fake, fake, fake, fake, None, None, fake]
+    args = [fake, -1.0, fake, None, fake, fake, fake, fake, fake, fake, fake, None, None, 0, None, fake]
     # layers outside [0, n_layers)
     assert lib.moe_decode_stack(ctypes.byref(s), 40, 9, *args, need, None) == RL_ERR_INVALID
     assert b"layers" in lib.rl_last_error()
@@ -95,6 +95,10 @@ def test_decode_stack_host_checks(lib):
     # misaligned router weights
     bad = list(args)
     bad[2] = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.moe_decode_stack(ctypes.byref(s), 0, 48, *bad, need, None) == RL_ERR_INVALID
+    # pregate beyond the 32 experts it can prefetch
+    bad = list(args)
+    bad[13] = 33
     assert lib.moe_decode_stack(ctypes.byref(s), 0, 48, *bad, need, None) == RL_ERR_INVALID
     # zero layers: nothing to do, no launch
     assert lib.moe_decode_stack(ctypes.byref(s), 48, 0, *args, need, None) == RL_OK

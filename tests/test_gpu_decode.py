@@ -224,7 +224,8 @@ def test_decode_stack_fused_equals_chain(stack_model):
     toks = [0, 77, w.tokens - 1]
     x = torch.from_numpy(synth.tokens(w, 0, w.tokens)).cuda()
     outs = {}
-    for mode in ("chain", "fused"):
+    hits = torch.zeros((len(toks), m.L), dtype=torch.int32, device="cuda")
+    for mode in ("chain", "fused", "fused_pregate"):
         b = engine.DecodeBuffers.make(m)
         hist = torch.zeros((len(toks), m.L, w.hidden), device="cuda")
         res = []
@@ -233,15 +234,33 @@ def test_decode_stack_fused_equals_chain(stack_model):
             if mode == "chain":
                 engine.enqueue_decode_token(m, b, x[t], y, stacked=True, keep_logits=True, x_hist=hist[i])
             else:
-                engine.enqueue_decode_token_fused(m, b, x[t], y, keep_logits=True, x_hist=hist[i])
+                pg = 32 if mode == "fused_pregate" else 0
+                engine.enqueue_decode_token_fused(m, b, x[t], y, keep_logits=True, x_hist=hist[i], pregate=pg,
+                                                  pregate_hits=hits[i] if pg else None)
             torch.cuda.synchronize()
             res.append([_bits(v) for v in (b.logits, b.ids, b.weights, b.slots, y)])
         assert b.ctrl.tolist() == [0x7FFFFFFF, 0] and int(b.miss.sum()) == 0
         outs[mode] = (res, _bits(hist), hist.double().cpu().numpy(), res[0][4].view(torch.float32).double().numpy())
-    for ra, rb in zip(outs["chain"][0], outs["fused"][0]):
-        for name, a_, b_ in zip(("logits", "ids", "weights", "slots", "y"), ra, rb):
-            assert torch.equal(a_, b_), name
-    assert torch.equal(outs["chain"][1], outs["fused"][1])
+    for other in ("fused", "fused_pregate"):   # the prefetch never changes a result
+        for ra, rb in zip(outs["chain"][0], outs[other][0]):
+            for name, a_, b_ in zip(("logits", "ids", "weights", "slots", "y"), ra, rb):
+                assert torch.equal(a_, b_), (other, name)
+        assert torch.equal(outs["chain"][1], outs[other][1])
+    # pre-gate hits: layer l's experts found in the top-32 of router l+1... applied at layer l-1,
+    # recomputed on the host from the GPU's own layer inputs (f32 logits; near ties may move one)
+    Hh = outs["fused_pregate"][2]
+    hits = hits.cpu().numpy()
+    for i in range(len(toks)):
+        ids = outs["fused_pregate"][0][i][1].numpy()
+        for l in range(1, m.L):
+            xn = oracle.rmsnorm(Hh[i][l - 1:l])
+            lg = oracle.router_logits(xn, o.router(l))[0]
+            pred = set(np.lexsort((np.arange(len(lg)), -lg))[:32].tolist())
+            want = len(set(ids[l].tolist()) & pred)
+            assert abs(int(hits[i, l]) - want) <= 1, (i, l, int(hits[i, l]), want)
+    rate = hits[:, 1:].mean() / w.top_k
+    print(f"pre-gate (top-32) hit rate {rate:.2f}")
+    assert rate > 0.5
     # the fused run of token 0 against the oracle, every 4th layer from its own layer inputs
     H = outs["fused"][2][0]
     y_last = outs["fused"][3]

@@ -325,8 +325,10 @@ def run_bounded_chunk(model: Model, b: PrefillBuffers, x: torch.Tensor, path: st
                       hist: dict | None = None) -> BoundedStats:
     """Prefill chunk through model.L stacked layers with bounded residency.
 
-    The chain is enqueued `window` layers at a time (default: all remaining layers); the
-    host then reads the flag.  If a layer f stopped the chain, its distinct missing experts
+    The chain is enqueued `window` layers at a time; the host then reads the flag.  With
+    window=None the window adapts: it starts at all layers, drops to one layer after an
+    early-out (the next layers are likely to stop too, and every layer enqueued past a stop is
+    a wasted launch) and doubles after each window that ran through.  If a layer f stopped the chain, its distinct missing experts
     are filled, its zero slots re-resolved, the flag reset, and the chain resumes with layer
     f's experts.  x is updated in place (x <- x + MoE(RMSNorm(x)) per layer).
     hist (optional): {"x": [L][T][H], "ids", "weights", "slots" ([L][T][K]), "logits" ([L][T][E])}
@@ -335,6 +337,7 @@ def run_bounded_chunk(model: Model, b: PrefillBuffers, x: torch.Tensor, path: st
     hist = hist or {}
     T, shp = x.shape[0], model.shape
     Lh = model.L
+    adaptive = window is None
     window = Lh if window is None else window
     stats = BoundedStats([0] * Lh, RL_NO_EARLY_OUT, [], [], 0, 0.0, 0)
     b.miss.zero_()
@@ -361,7 +364,11 @@ def run_bounded_chunk(model: Model, b: PrefillBuffers, x: torch.Tensor, path: st
         if f == RL_NO_EARLY_OUT:
             layer = end
             resume_experts = False
+            if adaptive:
+                window = min(Lh, 2 * window)
             continue
+        if adaptive:
+            window = 1
         # layer f selected absent experts: fill, re-resolve, reset the flag, resume at f's experts
         t0 = time.perf_counter()
         ids = b.ids.cpu().numpy()

@@ -250,8 +250,18 @@ __global__ void __launch_bounds__(kTcThreads2, 1) tc_gemm_kernel(PrefillArgs a, 
     const size_t rowb_q = matrix_bytes(1, a.H);  // bytes of an H-wide row (gate/up)
     const size_t matb = matrix_bytes(a.I, a.H);
     bool failed = false;
-    auto wait = [&](uint64_t *bar, uint32_t parity) {  // whole warp; bounded; sets the abort flag
+    // whole warp; bounded; sets the abort flag.  The per-chunk hand-offs between producers and
+    // the MMA issuer spin on test_wait (a suspended try_wait wakes too late for them); the
+    // long waits (a whole unit) suspend, so that waiting warps leave the issue slots free.
+    auto wait_spin = [&](uint64_t *bar, uint32_t parity) {
         if (!mbar_spin_warp(bar, parity)) {
+            if (lane == 0) atomicExch(abort_s, 1);
+            failed = true;
+        }
+        return !failed;
+    };
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+        if (!mbar_wait_warp(bar, parity)) {
             if (lane == 0) atomicExch(abort_s, 1);
             failed = true;
         }
@@ -338,7 +348,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1) tc_gemm_kernel(PrefillArgs a, 
             load_b(0, bv);
             for (int c = 0; c < nch && !failed; ++c, ++g) {
                 const int s = g % kTcStages;
-                if (g >= (uint32_t)kTcStages && !wait(&st_empty[s], ((g / kTcStages) - 1) & 1)) break;
+                if (g >= (uint32_t)kTcStages && !wait_spin(&st_empty[s], ((g / kTcStages) - 1) & 1)) break;
                 if (aborted()) { failed = true; break; }
                 uint8_t *dA = stg + s * (lay.stA + lay.stB);
                 uint8_t *dB = dA + lay.stA;
@@ -407,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1) tc_gemm_kernel(PrefillArgs a, 
             if (k >= 2 && !wait(&acc_empty[ab], ((k >> 1) - 1) & 1)) break;
             for (int c = 0; c < nch; ++c, ++g) {
                 const int s = g % kTcStages;
-                if (!wait(&st_full[s], (g / kTcStages) & 1)) break;
+                if (!wait_spin(&st_full[s], (g / kTcStages) & 1)) break;
                 if (lane == 0) {
                     tc::fence_after();
                     const int npad = meta[k & 1].npad;

@@ -349,6 +349,9 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
                              bar_dn);
             }
         }
+        // the computing warps start once every copy is issued: issued under their load the
+        // copies take about three times longer
+        __syncthreads();
         ex_issued = true;
 
         // ---------------- C: gate/up + SwiGLU of this CTA's pairs ----------------

@@ -56,7 +56,7 @@ __host__ __device__ inline int dn_unit(int I) { return I >= 2048 ? 1 : 2048 / I;
 
 struct StLayout {
     int rt_max, rmax, dmax, rowb, dtileb;
-    size_t o_x, o_rt, o_part, o_gu, o_dn, o_o, o_h, total;
+    size_t o_x, o_xt, o_rt, o_part, o_gu, o_dn, o_o, o_h, total;
     __host__ __device__ StLayout(int H, int E, int K, int I, int G) {
         rt_max = (E + G - 1) / G;
         const int U = gu_unit(H), units = K * I / U;
@@ -66,7 +66,8 @@ struct StLayout {
         rowb = (int)matrix_bytes(1, H);
         dtileb = (int)align_up(matrix_bytes(dmax, I), 16);
         o_x = kStHdr + kTabBytes;
-        o_rt = o_x + (size_t)H * sizeof(float);
+        o_xt = o_x + (size_t)H * sizeof(float);
+        o_rt = o_xt + (size_t)H * sizeof(float);  // x again, lane-transposed for the gate/up lanes
         o_part = o_rt + 2 * (size_t)rt_max * H * sizeof(float);  // two layers' router rows
         o_gu = o_part + align_up((size_t)rmax * 4 * sizeof(float), 16);
         o_dn = o_gu + 2 * (size_t)rmax * rowb;
@@ -83,7 +84,7 @@ struct StCta {
     int p0, p1, ka, kb, n0, n1;  // gate/up (expert, row) pairs: two segments (experts ka, kb)
     int q0, nq;              // down output rows
     int rowb, dtileb, dmax;
-    uint32_t o_x, o_rt, o_part, o_gu, o_dn, o_o, o_h;
+    uint32_t o_x, o_xt, o_rt, o_part, o_gu, o_dn, o_o, o_h;
     uint32_t rtb;            // bytes of one router buffer
 };
 
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
         C.rowb = lay.rowb;
         C.dtileb = lay.dtileb;
         C.dmax = lay.dmax;
-        C.o_x = (uint32_t)lay.o_x; C.o_rt = (uint32_t)lay.o_rt; C.o_part = (uint32_t)lay.o_part;
+        C.o_x = (uint32_t)lay.o_x; C.o_xt = (uint32_t)lay.o_xt; C.o_rt = (uint32_t)lay.o_rt; C.o_part = (uint32_t)lay.o_part;
         C.o_gu = (uint32_t)lay.o_gu; C.o_dn = (uint32_t)lay.o_dn; C.o_o = (uint32_t)lay.o_o; C.o_h = (uint32_t)lay.o_h;
         C.rtb = (uint32_t)((size_t)lay.rt_max * H * sizeof(float));
         for (int i = 0; i < kStBars; ++i) mbar_init(&bars[i], 1);
@@ -224,8 +225,15 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
         // ---------------- A: x_l, its scale, this CTA's logits ----------------
         {
             float *x_s = reinterpret_cast<float *>(smem + C.o_x);
-            for (int j = threadIdx.x; j < H / 4; j += kStThreads)
-                reinterpret_cast<float4 *>(x_s)[j] = __ldcg(reinterpret_cast<const float4 *>(a.x) + j);
+            float4 *xt_s = reinterpret_cast<float4 *>(smem + C.o_xt);
+            // x_s in order; xt_s lane-transposed for the gate/up lanes: float4 q of the slice of
+            // lane L of row half h (columns h H/SPLIT + L 8 GPL ...) sits at [h][q][L]
+            for (int j = threadIdx.x; j < H / 4; j += kStThreads) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.x) + j);
+                reinterpret_cast<float4 *>(x_s)[j] = v;
+                const int hf = H / 4 / SPLIT, h = j / hf, r = j % hf, L = r / (2 * GPL), q = r % (2 * GPL);
+                xt_s[(h * 2 * GPL + q) * 32 + L] = v;
+            }
             __syncthreads();
             if (warp == 0) {
                 const float r = a.eps >= 0.f ? rms_scale_warp(x_s, H, a.eps) : 1.f;
@@ -365,10 +373,10 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
             float xv[8 * GPL];
             {
                 const float r = *scale_s;
-                const float *x_s = reinterpret_cast<const float *>(smem + C.o_x);
+                const float4 *xt_s = reinterpret_cast<const float4 *>(smem + C.o_xt);
 #pragma unroll
                 for (int q = 0; q < 2 * GPL; ++q) {
-                    const float4 v = reinterpret_cast<const float4 *>(x_s + c0)[q];
+                    const float4 v = xt_s[(half * 2 * GPL + q) * 32 + lane];
                     xv[4 * q] = v.x * r; xv[4 * q + 1] = v.y * r; xv[4 * q + 2] = v.z * r; xv[4 * q + 3] = v.w * r;
                 }
             }
@@ -468,9 +476,9 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
             {
                 const int I = a.I, f4 = I / 4;
                 float4 *h_s = reinterpret_cast<float4 *>(smem + C.o_h);
-                for (int f = threadIdx.x; f < K * f4; f += kStThreads) {
-                    const int k = f / f4, r = f % f4, sl = r / (2 * DGPL), q = r % (2 * DGPL);
-                    h_s[k * f4 + q * LPR + sl] = __ldcg(reinterpret_cast<const float4 *>(a.h) + f);
+                for (int d = threadIdx.x; d < K * f4; d += kStThreads) {
+                    const int k = d / f4, r = d % f4, q = r / LPR, sl = r % LPR;
+                    h_s[d] = __ldcg(reinterpret_cast<const float4 *>(a.h) + k * f4 + sl * (2 * DGPL) + q);
                 }
                 __syncthreads();
             }

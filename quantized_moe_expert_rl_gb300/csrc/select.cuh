@@ -153,3 +153,79 @@ __device__ __forceinline__ void cta_topk(const float *lg, const uint64_t *__rest
 }
 
 }  // namespace rl
+
+namespace rl {
+
+// (ka, ia) comes before (kb, ib) in the selection order: larger key, then lower index
+__device__ __forceinline__ bool precedes(uint32_t ka, int ia, uint32_t kb, int ib) {
+    return ka > kb || (ka == kb && ia < ib);
+}
+
+// Top-k of up to 32 * NW logits with NW warps of one CTA, in few dependent steps.  Let m_w be
+// the largest key of warp w (lane = expert 32w + lane) and T the K-th largest of the m_w: the
+// K warps holding the K largest maxima give K keys >= T, so the K-th largest key overall is
+// >= T and every key of the top-K is >= T.  The keys >= T (usually a few tens) are gathered and
+// each is ranked exactly against the others in the order (logit descending, index ascending);
+// the K first are the selection, the same as warp_topk's.  cand_*: shared scratch of 32 * NW
+// entries; wm_s: NW words; sel: K entries; cnt_s: one word.  Lane r < K of every warp ends
+// with the r-th selection; the CTA is converged on return.  K <= NW.
+template <int NW>
+__device__ __forceinline__ void cta_topk_thr(const float *lg, const uint64_t *__restrict__ table_row, int E, int K,
+                                             uint32_t *cand_key, int *cand_id, uint64_t *cand_slot,
+                                             uint32_t *wm_s, int *sel, int *cnt_s, int &my_id, float &my_val,
+                                             uint64_t &my_slot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e = warp * 32 + lane;
+    uint32_t key = 0u;
+    if (warp < NW && e < E) key = order_key(__ldcg(lg + e));
+    if (threadIdx.x == 0) *cnt_s = 0;
+    if (warp < NW) {
+        const uint32_t m = __reduce_max_sync(kFull, key);
+        if (lane == 0) wm_s[warp] = m;
+    }
+    __syncthreads();
+    if (warp < NW) {
+        // T = the K-th largest warp maximum (ties by warp index, which only fixes who holds it)
+        const uint32_t mj = lane < NW ? wm_s[lane] : 0u;
+        int rank = 0;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const uint32_t mi = wm_s[i];
+            rank += (mi > mj || (mi == mj && i < lane)) ? 1 : 0;
+        }
+        const int who = __ffs(__ballot_sync(kFull, lane < NW && rank == K - 1)) - 1;
+        const uint32_t T = __shfl_sync(kFull, mj, who);
+        const bool cand = e < E && key >= T;
+        const unsigned mask = __ballot_sync(kFull, cand);
+        int base = 0;
+        if (lane == 0 && mask) base = atomicAdd(cnt_s, __popc(mask));
+        base = __shfl_sync(kFull, base, 0);
+        if (cand) {
+            const int at = base + __popc(mask & ((1u << lane) - 1u));
+            cand_key[at] = key;
+            cand_id[at] = e;
+            cand_slot[at] = __ldcg(table_row + e);
+        }
+    }
+    __syncthreads();
+    const int n = *cnt_s;
+    for (int c = threadIdx.x; c < n; c += blockDim.x) {
+        const uint32_t kc = cand_key[c];
+        const int ic = cand_id[c];
+        int r = 0;
+        for (int j = 0; j < n; ++j) r += precedes(cand_key[j], cand_id[j], kc, ic) ? 1 : 0;
+        if (r < K) sel[r] = c;
+    }
+    __syncthreads();
+    my_id = 0;
+    my_val = 0.f;
+    my_slot = 0;
+    if (lane < K) {
+        const int c = sel[lane];
+        my_id = cand_id[c];
+        my_val = key_value(cand_key[c]);
+        my_slot = cand_slot[c];
+    }
+}
+
+}  // namespace rl

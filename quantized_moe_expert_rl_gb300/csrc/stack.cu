@@ -44,9 +44,11 @@ constexpr int kStGuChunks = 2;
 constexpr int kStBars = 3 + 2 * kStGuChunks;  // [0,1] router rows, [2] down rows, [3..] gate/up chunks
 constexpr uint32_t kSpinCap = 1u << 22;       // global-memory polls (~1 us each): seconds
 constexpr int kStSelWarps = 16;               // selection warps: E <= 32 * 16
-constexpr int kStHdr = 4736;                  // barriers, scalars, CTA constants, selection scratch
+constexpr int kStHdr = 1024;                  // barriers, scalars, CTA constants, outputs of the selection
 constexpr int kStPredMax = 32;                // experts prefetched on the pre-gated prediction
 constexpr int kStCand = 16;                   // single-warp selection: candidates per lane (E <= 512)
+// selection scratch: keys, ids and table entries of up to 512 candidates, warp maxima, result, count
+constexpr int kStSelBytes = 512 * (4 + 4 + 8) + 64 + 64 + 16;
 // The warp that issues every bulk copy.  A memory fence waits for the bulk copies its own
 // thread has in flight, so the thread that runs the grid barrier (thread 0) never issues one.
 constexpr int kStProducer = kStWarps - 1;
@@ -56,7 +58,7 @@ __host__ __device__ inline int dn_unit(int I) { return I >= 2048 ? 1 : 2048 / I;
 
 struct StLayout {
     int rt_max, rmax, dmax, rowb, dtileb;
-    size_t o_x, o_xt, o_rt, o_part, o_gu, o_dn, o_o, o_h, total;
+    size_t o_x, o_xt, o_rt, o_part, o_gu, o_dn, o_o, o_h, o_sel, total;
     __host__ __device__ StLayout(int H, int E, int K, int I, int G) {
         rt_max = (E + G - 1) / G;
         const int U = gu_unit(H), units = K * I / U;
@@ -73,7 +75,8 @@ struct StLayout {
         o_dn = o_gu + 2 * (size_t)rmax * rowb;
         o_o = o_dn + (size_t)K * dtileb;
         o_h = o_o + align_up((size_t)K * dmax * sizeof(float), 16);
-        total = o_h + (size_t)K * I * sizeof(float);  // h of every expert, staged for the down rows
+        o_sel = o_h + (size_t)K * I * sizeof(float);  // h of every expert, staged for the down rows
+        total = o_sel + kStSelBytes;                     // selection scratch
     }
 };
 
@@ -84,7 +87,7 @@ struct StCta {
     int p0, p1, ka, kb, n0, n1;  // gate/up (expert, row) pairs: two segments (experts ka, kb)
     int q0, nq;              // down output rows
     int rowb, dtileb, dmax;
-    uint32_t o_x, o_xt, o_rt, o_part, o_gu, o_dn, o_o, o_h;
+    uint32_t o_x, o_xt, o_rt, o_part, o_gu, o_dn, o_o, o_h, o_sel;
     uint32_t rtb;            // bytes of one router buffer
 };
 
@@ -158,10 +161,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
     StCta &C = *reinterpret_cast<StCta *>(smem + 128);
     uint64_t *slots_s = reinterpret_cast<uint64_t *>(smem + 256);
     float *w_s = reinterpret_cast<float *>(smem + 384);
-    uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem + 512);
-    int *cand_id = reinterpret_cast<int *>(smem + 1536);
-    uint64_t *cand_slot = reinterpret_cast<uint64_t *>(smem + 2560);
-    int *pred_s = reinterpret_cast<int *>(smem + 4608);  // [kStPredMax] predicted ids of the next layer
+    int *pred_s = reinterpret_cast<int *>(smem + 512);  // [kStPredMax] predicted ids of the next layer
     uint4 *tab = reinterpret_cast<uint4 *>(smem + kStHdr);
     constexpr int H = NV * 128;
     constexpr int U = H >= 2048 ? 1 : 2048 / H;  // gu_unit(H)
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
         C.dtileb = lay.dtileb;
         C.dmax = lay.dmax;
         C.o_x = (uint32_t)lay.o_x; C.o_xt = (uint32_t)lay.o_xt; C.o_rt = (uint32_t)lay.o_rt; C.o_part = (uint32_t)lay.o_part;
-        C.o_gu = (uint32_t)lay.o_gu; C.o_dn = (uint32_t)lay.o_dn; C.o_o = (uint32_t)lay.o_o; C.o_h = (uint32_t)lay.o_h;
+        C.o_gu = (uint32_t)lay.o_gu; C.o_dn = (uint32_t)lay.o_dn; C.o_o = (uint32_t)lay.o_o; C.o_h = (uint32_t)lay.o_h; C.o_sel = (uint32_t)lay.o_sel;
         C.rtb = (uint32_t)((size_t)lay.rt_max * H * sizeof(float));
         for (int i = 0; i < kStBars; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -290,8 +290,13 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
             int my_id;
             float my_val;
             uint64_t slot;
-            cta_topk<kStSelWarps>(a.lg, a.table + (size_t)l * a.E, a.E, K, cand_key, cand_id, cand_slot, my_id,
-                                  my_val, slot);
+            {
+                uint8_t *sb = smem + C.o_sel;
+                cta_topk_thr<kStSelWarps>(a.lg, a.table + (size_t)l * a.E, a.E, K, reinterpret_cast<uint32_t *>(sb),
+                                          reinterpret_cast<int *>(sb + 2048), reinterpret_cast<uint64_t *>(sb + 4096),
+                                          reinterpret_cast<uint32_t *>(sb + 8192), reinterpret_cast<int *>(sb + 8256),
+                                          reinterpret_cast<int *>(sb + 8320), my_id, my_val, slot);
+            }
             if (warp == 0) {
                 const float w = topk_weight(my_val, K);
                 const int nmiss = __popc(__ballot_sync(kFull, lane < K && slot == 0));

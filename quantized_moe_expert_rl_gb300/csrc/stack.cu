@@ -330,9 +330,11 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
         }
         __syncthreads();
         if (*stop_s) break;
+        // the last warp issues the gate/up copies, the one before it the down copies (two
+        // issuing warps halve the issue time)
         if (warp == kStProducer) {
             fence_proxy_async_smem();
-            const int K = a.K, I = a.I, rowb = C.rowb;
+            const int I = a.I, rowb = C.rowb;
             const size_t matb = matrix_bytes(I, H);
             // gate/up: lane i < 2 * kStGuChunks issues chunk (segment i / kStGuChunks, part
             // i % kStGuChunks): its gate rows and its up rows, completion on bar_gu[i]
@@ -350,6 +352,10 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
                     bulk_g2s(gdst + (size_t)n * rowb, base + matb + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
                 }
             }
+        } else if (warp == kStProducer - 1) {
+            fence_proxy_async_smem();
+            const int K = a.K, I = a.I;
+            const size_t matb = matrix_bytes(I, H);
             // down: rows [q0, q0 + nq) of every selected expert, completion on bar_dn
             const int nq = C.nq;
             if (nq > 0) {

@@ -119,54 +119,94 @@ __global__ void __launch_bounds__(kR1Threads) route1_kernel(const float *__restr
 }
 
 // ---------------------------------------------------------------------------------------------
-// Many tokens: 64 x 64 (tokens x experts) tiles, K step 16, 4 x 4 outputs per thread.
+// Many tokens, register-tiled: logits[t][e] = sum_h xn[t][h] W[e][h] with a 128 x 128 tile per
+// CTA, 8 x 8 outputs per thread (rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, columns likewise
+// from tx), K in steps of 8 staged k-major in shared memory (double-buffered, the next step's
+// global loads in flight during the current one).  Split-K over blockIdx.z when the tiles alone
+// cannot fill the GPU: slice z writes its partial sums, and router_reduce_kernel adds the
+// slices in order (then the bias).  Every output is one thread's sequential f32 FMA chain per
+// slice, so the result is deterministic.
 // ---------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) router_gemm_kernel(const float *__restrict__ xn, const float *__restrict__ W,
-                                                          const float *__restrict__ bias,
-                                                          float *__restrict__ logits, int T, int H, int E,
-                                                          const int32_t *ctrl, int layer) {
+constexpr int kSgT = 128, kSgBK = 8, kSgPad = 4;
+
+__global__ void __launch_bounds__(256) router_sgemm_kernel(const float *__restrict__ xn, const float *__restrict__ W,
+                                                           const float *__restrict__ bias, float *__restrict__ out,
+                                                           int T, int H, int E, int kslice, const int32_t *ctrl,
+                                                           int layer) {
     if (ld_ctrl(ctrl) < layer) return;
-    __shared__ float As[16][68];
-    __shared__ float Bs[16][68];
+    __shared__ __align__(16) float As[2][kSgBK][kSgT + kSgPad];
+    __shared__ __align__(16) float Bs[2][kSgBK][kSgT + kSgPad];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int t_base = blockIdx.y * 64, e_base = blockIdx.x * 64;
-    const int lrow = tid >> 2, lk = (tid & 3) * 4;
-    float acc[4][4] = {};
-    for (int k0 = 0; k0 < H; k0 += 16) {
-        {
-            const int t = t_base + lrow;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < T) v = *reinterpret_cast<const float4 *>(xn + (size_t)t * H + k0 + lk);
-            As[lk + 0][lrow] = v.x; As[lk + 1][lrow] = v.y; As[lk + 2][lrow] = v.z; As[lk + 3][lrow] = v.w;
-            const int e = e_base + lrow;
-            float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < E) w = *reinterpret_cast<const float4 *>(W + (size_t)e * H + k0 + lk);
-            Bs[lk + 0][lrow] = w.x; Bs[lk + 1][lrow] = w.y; Bs[lk + 2][lrow] = w.z; Bs[lk + 3][lrow] = w.w;
+    const int t0 = blockIdx.y * kSgT, e0 = blockIdx.x * kSgT;
+    const int k_lo = blockIdx.z * kslice, k_hi = k_lo + kslice;
+    // loader: thread -> (row tid / 2, 4 consecutive k at (tid % 2) * 4) of both tiles
+    const int lr = tid >> 1, lk = (tid & 1) * 4;
+    const bool a_ok = t0 + lr < T, b_ok = e0 + lr < E;
+    const float *a_src = xn + (size_t)(a_ok ? t0 + lr : 0) * H + lk;
+    const float *b_src = W + (size_t)(b_ok ? e0 + lr : 0) * H + lk;
+    float4 av = make_float4(0.f, 0.f, 0.f, 0.f), bv = av;
+    if (a_ok) av = *reinterpret_cast<const float4 *>(a_src + k_lo);
+    if (b_ok) bv = *reinterpret_cast<const float4 *>(b_src + k_lo);
+    auto stage = [&](int buf) {
+        As[buf][lk + 0][lr] = av.x; As[buf][lk + 1][lr] = av.y; As[buf][lk + 2][lr] = av.z; As[buf][lk + 3][lr] = av.w;
+        Bs[buf][lk + 0][lr] = bv.x; Bs[buf][lk + 1][lr] = bv.y; Bs[buf][lk + 2][lr] = bv.z; Bs[buf][lk + 3][lr] = bv.w;
+    };
+    stage(0);
+    __syncthreads();
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    int buf = 0;
+    for (int k0 = k_lo; k0 < k_hi; k0 += kSgBK) {
+        const bool more = k0 + kSgBK < k_hi;
+        if (more) {  // next step's loads in flight during this step's FMAs
+            if (a_ok) av = *reinterpret_cast<const float4 *>(a_src + k0 + kSgBK);
+            if (b_ok) bv = *reinterpret_cast<const float4 *>(b_src + k0 + kSgBK);
         }
-        __syncthreads();
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            float a[4], b[4];
+        for (int kk = 0; kk < kSgBK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][kk][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][kk][64 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][64 + tx * 4]);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
-        __syncthreads();
+        if (more) {
+            stage(buf ^ 1);
+            __syncthreads();
+            buf ^= 1;
+        }
     }
+    float *o = out + (size_t)blockIdx.z * T * E;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t_base + ty + 16 * i;
+    for (int i = 0; i < 8; ++i) {
+        const int t = t0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
         if (t >= T) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e_base + tx + 16 * j;
-            if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+        for (int j = 0; j < 8; ++j) {
+            const int e = e0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
+            if (e < E) o[(size_t)t * E + e] = gridDim.z == 1 ? acc[i][j] + (bias ? bias[e] : 0.f) : acc[i][j];
         }
+    }
+}
+
+// logits = (slice 0 + slice 1 + ...) + bias, slices added in order
+__global__ void __launch_bounds__(256) router_reduce_kernel(const float *__restrict__ part, const float *__restrict__ bias,
+                                                            float *__restrict__ logits, int T, int E, int S,
+                                                            const int32_t *ctrl, int layer) {
+    if (ld_ctrl(ctrl) < layer) return;
+    const size_t n = (size_t)T * E;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        float v = part[i];
+        for (int z = 1; z < S; ++z) v += part[(size_t)z * n + i];
+        logits[i] = v + (bias ? bias[i % E] : 0.f);
     }
 }
 
@@ -190,12 +230,27 @@ __global__ void resolve_slots_kernel(const int32_t *__restrict__ ids, const uint
     slots[i] = (e >= 0 && e < E) ? table_row[e] : 0;
 }
 
-struct RouteWs {  // [counter (256 B) | logits T*E f32 | normalised input T*H f32 (T > 1 with norm)]
-    size_t logits, xn, total;
+constexpr int kSgMaxSplit = 8, kSgMaxSms = 256;
+// split-K factor of the many-token router GEMM: enough CTAs for `sms` SMs, K slices that stay
+// multiples of the K step.  The workspace is sized with kSgMaxSms, so it does not depend on the
+// device it was sized on.
+static int router_splits(int T, int E, int H, int sms) {
+    if (T <= 1) return 1;
+    const int tiles = ((T + kSgT - 1) / kSgT) * ((E + kSgT - 1) / kSgT);
+    sms = std::min(sms, kSgMaxSms);
+    int S = 1;
+    while (S < kSgMaxSplit && tiles * S * 2 <= sms && H % (kSgBK * S * 2) == 0 && H / (S * 2) >= 64) S *= 2;
+    return S;
+}
+
+struct RouteWs {  // [counter (256 B) | logits T*E | normalised input T*H (T > 1 with norm) | split-K partials]
+    size_t logits, xn, part, total;
     RouteWs(int T, int E, int H, bool norm) {
         logits = 256;
         xn = logits + align_up((size_t)T * E * sizeof(float), 256);
-        total = xn + (norm && T > 1 ? align_up((size_t)T * H * sizeof(float), 256) : 0);
+        part = xn + (norm && T > 1 ? align_up((size_t)T * H * sizeof(float), 256) : 0);
+        const int S = router_splits(T, E, H, kSgMaxSms);
+        total = part + (S > 1 ? align_up((size_t)S * T * E * sizeof(float), 256) : 0);
     }
 };
 
@@ -292,8 +347,17 @@ extern "C" rl_status rl_route(const rl_moe_shape *shp, int32_t layer, int32_t T,
         rmsnorm_kernel<<<T, 256, 0, s>>>(x, xn, H, norm_eps);
         src = xn;
     }
-    router_gemm_kernel<<<dim3((E + 63) / 64, (T + 63) / 64), 256, 0, s>>>(src, w_router, bias, logits, T, H, E, ctrl,
-                                                                        layer);
+    {
+        const int S = router_splits(T, E, H, sm_count());
+        float *part = S > 1 ? reinterpret_cast<float *>(w8 + L.part) : logits;
+        router_sgemm_kernel<<<dim3((E + kSgT - 1) / kSgT, (T + kSgT - 1) / kSgT, S), 256, 0, s>>>(
+            src, w_router, bias, part, T, H, E, H / S, ctrl, layer);
+        if (S > 1) {
+            const size_t n = (size_t)T * E;
+            router_reduce_kernel<<<(int)std::min<size_t>((n + 255) / 256, 2048), 256, 0, s>>>(part, bias, logits, T, E,
+                                                                                            S, ctrl, layer);
+        }
+    }
     const dim3 g((T + 7) / 8), b(256);
     if (E <= 32) route_select_kernel<1><<<g, b, 0, s>>>(logits, row, ids, weights, slots, miss_l, ctrl, layer, T, E, K);
     else if (E <= 64) route_select_kernel<2><<<g, b, 0, s>>>(logits, row, ids, weights, slots, miss_l, ctrl, layer, T, E, K);

@@ -74,6 +74,7 @@ typedef enum rl_status {
 #define RL_DEVERR_WAIT_TIMEOUT 2 /* a bounded on-chip wait ran out of iterations */
 #define RL_DEVERR_BAD_ID 4       /* an expert id outside [0, n_experts) was read */
 #define RL_DEVERR_MISSING 8      /* an expert kernel met a zero (absent) slot */
+#define RL_DEVERR_RANGE 16       /* moe_decode_stack: a router partial sum outside the fixed-point range */
 
 /* (host) model shape, passed by pointer to every call */
 typedef struct rl_moe_shape {
@@ -184,7 +185,12 @@ rl_status moe_decode_static(const rl_moe_shape *shp, int32_t layer, const float 
  * item 1: at the first layer f that selects an absent expert, ids/weights/slots[f] and miss[f]
  * are written, ctrl[0] = min(ctrl[0], f), and the launch stops with x = x_f (the input of
  * layer f), so the caller can fill, rl_resolve_slots(f), moe_decode(f) and resume at f + 1.
- * Results are bit-identical to the per-layer chain rl_route + moe_decode (same arithmetic).
+ * The expert arithmetic, the RMSNorm scale and the selection are those of the per-layer chain
+ * rl_route + moe_decode; the router logits are summed differently: every CTA adds the dots of
+ * its slice of x into 64-bit fixed-point accumulators (exact, order-independent sums of f32
+ * partials of |p| < 2^19, resolution 2^-36), and logit = rs * sum + bias.  A partial outside
+ * that range sets RL_DEVERR_RANGE (and counts as 0).  Results do not depend on how the layers
+ * are split between calls.
  * x [H] f32 in/out (16-byte aligned); w_router [n_layers][E][H] f32; bias [n_layers][E] f32 or
  * NULL; residency [n_layers][E]; codebook int8 [256][8]; ids int32, weights f32, slots uint64:
  * [n_layers][K] (rows of the run are written); miss uint32 [n_layers] (accumulated);

@@ -112,13 +112,13 @@ __global__ void __launch_bounds__(kGuThreads) dec_gateup_kernel(const float *__r
             }
         }
     }
-    __syncthreads();  // x staged, ok_s written
+    cta_sync();  // x staged, ok_s written; warp 0 rejoined after its lane-dependent copy issue
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (NORM && warp == 0) {
         const float r = rms_scale_warp(x_s, H, eps);
         if (lane == 0) *scale_s = r;
     }
-    __syncthreads();
+    cta_sync();
     if (!*ok_s) return;
     pdl_trigger();
     const int half = warp % SPLIT, team = warp / SPLIT;
@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kGuThreads) dec_gateup_kernel(const float *__r
                 part[((q - p0) * 2 + half) * 2 + 1] = uv2;
             }
         }
+        __syncwarp();  // rejoin before the next row's shuffles (see cta_sync)
     }
     if (timed_out && lane == 0) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
     // Warm L2 with the down matrices the next kernel reads (CTA c takes the c-th slice of every
@@ -261,6 +262,7 @@ __global__ void dec_down_kernel(const uint64_t *__restrict__ slots, const float 
     for (int rr = r_lo + sub; rr < r_lo + kDnRows / 2; rr += kRowsPerPass) {
         const float o = down_row<GPL, LPR>(tile, rr, I, sl, hv, tabc);
         if (sl == 0) o_s[k * kDnRows + rr] = o;
+        __syncwarp();
     }
     __syncthreads();
     if (threadIdx.x < kDnRows) {

@@ -57,7 +57,9 @@ __device__ __forceinline__ float down_row(const uint8_t *tile, int rr, int I, in
 // sum_k w_k * o_k in selection order (o_k at o[k * stride])
 __device__ __forceinline__ float ordered_combine(const float *w, const float *o, int stride, int K) {
     float acc = 0.f;
-    for (int k = 0; k < K; ++k) acc = fmaf(w[k], o[k * stride], acc);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        if (k < K) acc = fmaf(w[k], o[k * stride], acc);
     return acc;
 }
 

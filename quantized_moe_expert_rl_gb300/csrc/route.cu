@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kR1Threads) route1_kernel(const float *__restr
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s(Ws, W + (size_t)e0 * H, bytes, bar);
     }
-    __syncthreads();
+    cta_sync();  // also rejoins warp 0 (its shuffles follow)
     pdl_wait();
     const bool skip = ld_ctrl(ctrl) < layer;
     float4 xv[NV];
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kR1Threads) route1_kernel(const float *__restr
             if (lane == 0) *scale_s = r;
         }
     }
-    __syncthreads();
+    cta_sync();
     // the router rows must have landed before the CTA may exit, whether it skips or not
     if (!mbar_wait_warp(bar, 0)) {
         if (threadIdx.x == 0) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(kR1Threads) route1_kernel(const float *__restr
     __syncthreads();
     if (!*last_s) return;
     __threadfence();
+    __syncwarp();  // warp 0 rejoined after thread 0's arrival (warp_select is all shuffles and votes)
     if (warp == 0) {
         warp_select<C>(logits, table_row, ids, weights, slots, miss_l, ctrl, layer, E, K);
         if (lane == 0) *counter = 0u;  // every call leaves the counter at zero

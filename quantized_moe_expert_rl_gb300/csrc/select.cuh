@@ -14,6 +14,8 @@
 
 namespace rl {
 
+constexpr int kMaxK = 16;  // largest top-k the library accepts
+
 __device__ __forceinline__ uint32_t order_key(float v) {
     const uint32_t b = __float_as_uint(v + 0.0f);  // -0.0 + 0.0 = +0.0
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
@@ -23,22 +25,23 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 }
 
 // After the call lane r < K holds the r-th selected expert (my_id) and its logit (my_val).
-// The logits are read through L2 (they may come from other CTAs).
-template <int C>
-__device__ __forceinline__ void warp_topk(const float *lg, int E, int K, int &my_id, float &my_val) {
+// key_of(e) gives the key of expert e (0 for an absent one), for e < 32 * C.  K <= MAXK <= 32.
+template <int C, int MAXK = kMaxK, class KeyOf>
+__device__ __forceinline__ void warp_topk_by(KeyOf key_of, int K, int &my_id, float &my_val) {
     const int lane = threadIdx.x & 31;
     uint32_t key[C];
     uint32_t best = 0u;
     int bi = 0;
 #pragma unroll
     for (int i = 0; i < C; ++i) {
-        const int e = lane * C + i;
-        key[i] = e < E ? order_key(__ldcg(lg + e)) : 0u;
+        key[i] = key_of(lane * C + i);
         if (key[i] > best) { best = key[i]; bi = i; }
     }
     my_id = 0;
     my_val = 0.f;
-    for (int r = 0; r < K; ++r) {
+#pragma unroll
+    for (int r = 0; r < MAXK; ++r) {
+        if (r >= K) break;
         const uint32_t m = __reduce_max_sync(kFull, best);
         const int wl = __ffs(__ballot_sync(kFull, best == m)) - 1;
         const int wi = __shfl_sync(kFull, bi, wl);
@@ -52,7 +55,14 @@ __device__ __forceinline__ void warp_topk(const float *lg, int E, int K, int &my
                 if (key[i] > best) { best = key[i]; bi = i; }
             }
         }
+        __syncwarp();  // rejoin before the next round's votes (see cta_sync)
     }
+}
+
+// warp_topk_by on E logits read through L2 (they may come from other CTAs)
+template <int C>
+__device__ __forceinline__ void warp_topk(const float *lg, int E, int K, int &my_id, float &my_val) {
+    warp_topk_by<C>([&](int e) { return e < E ? order_key(__ldcg(lg + e)) : 0u; }, K, my_id, my_val);
 }
 
 // w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0), the sum taken in selection order; lane k < K
@@ -62,7 +72,13 @@ __device__ __forceinline__ float topk_weight(float my_val, int K) {
     const float l0 = __shfl_sync(kFull, my_val, 0);
     const float ex = lane < K ? expf(my_val - l0) : 0.f;
     float tot = 0.f;
-    for (int k = 0; k < K; ++k) tot += __shfl_sync(kFull, ex, k);
+    // unrolled to the largest K (16) with the adds predicated: a loop over a run-time K with a
+    // shuffle in its body ran about ten times slower
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        const float v = __shfl_sync(kFull, ex, k);
+        if (k < K) tot += v;
+    }
     return lane < K ? ex / tot : 0.f;
 }
 
@@ -83,72 +99,11 @@ __device__ __forceinline__ void warp_select(const float *lg, const uint64_t *__r
         slot = table_row[my_id];
         slots[lane] = slot;
     }
+    __syncwarp();
     const int nmiss = __popc(__ballot_sync(kFull, lane < K && slot == 0));
     if (lane == 0 && nmiss > 0) {
         atomicAdd(miss_l, (uint32_t)nmiss);
         atomicMin(ctrl, layer);
-    }
-}
-
-}  // namespace rl
-
-namespace rl {
-
-// Top-k of up to 32 * NW logits with NW warps of one CTA (the fused decode stack runs it in
-// every CTA).  Level 1: warp w owns experts 32w .. 32w+31 (lane = expert within the warp) and
-// takes its own top-k by K rounds of warp max, the lowest lane winning among equal keys, so
-// each warp's list is ordered by (logit descending, index ascending).  The residency-table
-// entry of every expert is loaded together with its logit.  Level 2 (warp 0): a K-round merge
-// of the NW lists, lane j holding the head of list j; equal keys go to the lowest list, whose
-// experts have the lower indices.  The result (ids, logits and their table entries) is the
-// same as warp_topk's, since both follow the one total order (logit descending, index
-// ascending).  cand_key/cand_id/cand_slot: shared scratch of NW * K entries.  Lane r < K of
-// warp 0 ends with the r-th selection; the CTA is converged on return.
-template <int NW>
-__device__ __forceinline__ void cta_topk(const float *lg, const uint64_t *__restrict__ table_row, int E, int K,
-                                         uint32_t *cand_key, int *cand_id, uint64_t *cand_slot, int &my_id,
-                                         float &my_val, uint64_t &my_slot) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (warp < NW) {
-        const int e = warp * 32 + lane;
-        uint32_t key = 0u;
-        uint64_t slot = 0;
-        if (e < E) {
-            key = order_key(__ldcg(lg + e));
-            slot = __ldcg(table_row + e);
-        }
-        for (int r = 0; r < K; ++r) {
-            const uint32_t m = __reduce_max_sync(kFull, key);
-            const int wl = __ffs(__ballot_sync(kFull, key == m)) - 1;
-            if (lane == wl) {
-                cand_key[warp * K + r] = m;
-                cand_id[warp * K + r] = e;
-                cand_slot[warp * K + r] = slot;
-                key = 0u;
-            }
-        }
-    }
-    __syncthreads();
-    my_id = 0;
-    my_val = 0.f;
-    my_slot = 0;
-    if (warp == 0) {
-        int ptr = 0;
-        uint32_t hk = lane < NW ? cand_key[lane * K] : 0u;
-        for (int r = 0; r < K; ++r) {
-            const uint32_t m = __reduce_max_sync(kFull, hk);
-            const int wl = __ffs(__ballot_sync(kFull, hk == m)) - 1;
-            const int at = __shfl_sync(kFull, wl * K + ptr, wl);
-            if (lane == r) {
-                my_id = cand_id[at];
-                my_val = key_value(m);
-                my_slot = cand_slot[at];
-            }
-            if (lane == wl) {
-                ++ptr;
-                hk = (ptr < K && lane < NW) ? cand_key[lane * K + ptr] : 0u;
-            }
-        }
     }
 }
 
@@ -161,8 +116,10 @@ __device__ __forceinline__ bool precedes(uint32_t ka, int ia, uint32_t kb, int i
     return ka > kb || (ka == kb && ia < ib);
 }
 
-// Top-k of up to 32 * NW logits with NW warps of one CTA, in few dependent steps.  Let m_w be
-// the largest key of warp w (lane = expert 32w + lane) and T the K-th largest of the m_w: the
+// Top-k of up to 32 * NW logits with NW warps of one CTA (the fused decode stack runs it in
+// every CTA), in few dependent steps.  Thread 32w + lane passes `key`, the key of expert
+// 32w + lane (0 when absent; the threads of warps >= NW pass 0).  Let m_w be
+// the largest key of warp w and T the K-th largest of the m_w: the
 // K warps holding the K largest maxima give K keys >= T, so the K-th largest key overall is
 // >= T and every key of the top-K is >= T.  The keys >= T (usually a few tens) are gathered and
 // each is ranked exactly against the others in the order (logit descending, index ascending);
@@ -170,20 +127,19 @@ __device__ __forceinline__ bool precedes(uint32_t ka, int ia, uint32_t kb, int i
 // entries; wm_s: NW words; sel: K entries; cnt_s: one word.  Lane r < K of every warp ends
 // with the r-th selection; the CTA is converged on return.  K <= NW.
 template <int NW>
-__device__ __forceinline__ void cta_topk_thr(const float *lg, const uint64_t *__restrict__ table_row, int E, int K,
+__device__ __forceinline__ void cta_topk_thr(uint32_t key, const uint64_t *__restrict__ table_row, int E, int K,
                                              uint32_t *cand_key, int *cand_id, uint64_t *cand_slot,
                                              uint32_t *wm_s, int *sel, int *cnt_s, int &my_id, float &my_val,
                                              uint64_t &my_slot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int e = warp * 32 + lane;
-    uint32_t key = 0u;
-    if (warp < NW && e < E) key = order_key(__ldcg(lg + e));
+    if (warp >= NW || e >= E) key = 0u;
     if (threadIdx.x == 0) *cnt_s = 0;
     if (warp < NW) {
         const uint32_t m = __reduce_max_sync(kFull, key);
         if (lane == 0) wm_s[warp] = m;
     }
-    __syncthreads();
+    cta_sync();
     if (warp < NW) {
         // T = the K-th largest warp maximum (ties by warp index, which only fixes who holds it)
         const uint32_t mj = lane < NW ? wm_s[lane] : 0u;
@@ -199,6 +155,7 @@ __device__ __forceinline__ void cta_topk_thr(const float *lg, const uint64_t *__
         const unsigned mask = __ballot_sync(kFull, cand);
         int base = 0;
         if (lane == 0 && mask) base = atomicAdd(cnt_s, __popc(mask));
+        __syncwarp();
         base = __shfl_sync(kFull, base, 0);
         if (cand) {
             const int at = base + __popc(mask & ((1u << lane) - 1u));
@@ -207,16 +164,17 @@ __device__ __forceinline__ void cta_topk_thr(const float *lg, const uint64_t *__
             cand_slot[at] = __ldcg(table_row + e);
         }
     }
-    __syncthreads();
+    cta_sync();
     const int n = *cnt_s;
     for (int c = threadIdx.x; c < n; c += blockDim.x) {
         const uint32_t kc = cand_key[c];
         const int ic = cand_id[c];
         int r = 0;
+#pragma unroll 4
         for (int j = 0; j < n; ++j) r += precedes(cand_key[j], cand_id[j], kc, ic) ? 1 : 0;
         if (r < K) sel[r] = c;
     }
-    __syncthreads();
+    cta_sync();
     my_id = 0;
     my_val = 0.f;
     my_slot = 0;
@@ -226,6 +184,7 @@ __device__ __forceinline__ void cta_topk_thr(const float *lg, const uint64_t *__
         my_val = key_value(cand_key[c]);
         my_slot = cand_slot[c];
     }
+    __syncwarp();
 }
 
 }  // namespace rl

@@ -11,28 +11,38 @@
 //
 // Design: one CTA per SM (cooperative launch, so all CTAs are co-resident), 16 warps each.
 // Every CTA owns a fixed slice of each phase's work for the whole launch:
-//   router rows [e0, e0+nr), gate/up (expert, row) pairs [p0, p1), down output rows [q0, q0+nq).
-// Per layer:
-//   A  x_l (L2) -> RMSNorm scale; logits of the CTA's router rows, whose weights were copied
-//      into shared memory during the previous layer (they do not depend on x);
-//      grid barrier
-//   B  every CTA selects the top-k from all logits itself (the same code on the same data
-//      gives the same ids everywhere, so no further exchange is needed); CTA 0 writes the
-//      outputs, the miss count and the flag; a miss (or the flag) stops every CTA.  Then the
-//      CTA's gate/up rows and down rows of the K selected experts are copied into shared
-//      memory with bulk asynchronous copies, all at once;
-//   C  gate/up + SwiGLU of the CTA's pairs -> h (L2); the next layer's router rows are
-//      requested;  grid barrier
-//   D  the CTA's rows of every expert's down projection, the ordered combine and the
-//      residual -> x_{l+1} (L2);  grid barrier.
-// The arithmetic of every row, the RMSNorm scale and the selection are the very functions the
-// per-layer kernels (rl_route, moe_decode) use, so the result is bit-identical to that chain.
+//   gate/up (expert, row) pairs [p0, p1); down output rows [q0, q0+nq), i.e. its slice of x.
+// The router is split by columns, not rows: CTA b holds columns [q0, q0+nq) of every router row
+// in shared memory (copied a layer ahead; they do not depend on x) and, as soon as its slice of
+// x_l is final, adds its partial dot of every row into the layer's logit accumulators.  The
+// accumulators are 64-bit fixed point (2^-36 resolution), so the sum is exact up to the
+// rounding of each f32 partial and does not depend on the order in which the CTAs arrive.  With
+// rs the RMSNorm scale, logit_e = rs * sum_h W[e][h] x[h] + bias_e, the same linear map as
+// W (rs x).  This takes the router off the critical path: no barrier separates x_l from the
+// selection other than the one that publishes x_l itself.
+// Per launch: CTA 0 clears the accumulators, grid barrier, every CTA adds its dots on x_layer0,
+// grid barrier.  Per layer:
+//   B  x_l (L2) -> RMSNorm scale; logits from the accumulators; every CTA selects the top-k
+//      itself (the same code on the same data gives the same ids everywhere, so no further
+//      exchange is needed); CTA 0 writes the outputs, the miss count and the flag; a miss (or
+//      the flag) stops every CTA.  Then the CTA's gate/up rows and down rows of the K selected
+//      experts are copied into shared memory with bulk asynchronous copies, all at once;
+//   C  gate/up + SwiGLU of the CTA's pairs -> h (L2);  grid barrier
+//   D  the CTA's rows of every expert's down projection, the ordered combine and the residual
+//      -> its slice of x_{l+1} (L2), then its router dots of layer l+1 on that slice;
+//      grid barrier.
+// The arithmetic of every expert row, of the RMSNorm scale and of the selection is the one the
+// per-layer kernels (rl_route, moe_decode) use; the logits differ from rl_route's only by the
+// order of summation (rl_route: one f32 dot per row).
 //
 // Grid barrier: a 64-bit arrival counter in the workspace that only ever grows.  The first
 // arrival of a launch rounds its value down to a multiple of the grid size to find the base,
 // so no reset is needed between launches.  Every spin is bounded: on expiry the CTA sets
 // RL_DEVERR_WAIT_TIMEOUT, waits (bounded) for its own copies in flight and returns; the other
 // CTAs then time out at their next barrier.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "decode_rows.cuh"
 #include "select.cuh"
 
@@ -41,9 +51,9 @@ namespace rl {
 constexpr int kStThreads = 512;
 constexpr int kStWarps = kStThreads / 32;
 constexpr int kStGuChunks = 2;
-constexpr int kStBars = 3 + 2 * kStGuChunks;  // [0,1] router rows, [2] down rows, [3..] gate/up chunks
+constexpr int kStBars = 2 + 2 * kStGuChunks;  // [0] down rows, [1] router columns, [2..] gate/up chunks
 constexpr uint32_t kSpinCap = 1u << 22;       // global-memory polls (~1 us each): seconds
-constexpr int kStSelWarps = 16;               // selection warps: E <= 32 * 16
+constexpr int kStSelWarps = 16;               // selection warps: E <= 32 * 16, one expert per thread
 constexpr int kStHdr = 1024;                  // barriers, scalars, CTA constants, outputs of the selection
 constexpr int kStPredMax = 32;                // experts prefetched on the pre-gated prediction
 constexpr int kStCand = 16;                   // single-warp selection: candidates per lane (E <= 512)
@@ -52,25 +62,41 @@ constexpr int kStSelBytes = 512 * (4 + 4 + 8) + 64 + 64 + 16;
 // The warp that issues every bulk copy.  A memory fence waits for the bulk copies its own
 // thread has in flight, so the thread that runs the grid barrier (thread 0) never issues one.
 constexpr int kStProducer = kStWarps - 1;
+// Router partial sums in 64-bit fixed point, value * 2^36 rounded to an integer: a partial is
+// limited to |p| < 2^19, so the sum of up to 2^8 of them (one per CTA) stays inside int64.
+constexpr float kFixScale = 68719476736.0f;         // 2^36
+constexpr float kFixInv = 1.4551915228366852e-11f;  // 2^-36
+constexpr float kFixMax = 524288.0f;                // 2^19
+constexpr int kStMaxGrid = 256;
 
 // down rows handled together so that every copy starts on a block boundary (rows * I % 2048 == 0)
 __host__ __device__ inline int dn_unit(int I) { return I >= 2048 ? 1 : 2048 / I; }
+// a CTA's slice of x (its down rows) is made of whole down units and of whole 8-float groups,
+// so that its router columns are whole 32-byte DRAM sectors; CTA b owns rows [b dmax, b dmax +
+// dmax) (fewer for the last, none past H), so every busy CTA takes the same column box
+__host__ __device__ inline int dq_unit(int I) { return dn_unit(I) > 8 ? dn_unit(I) : 8; }
+// router rows per column box (a tensor copy moves at most 256 rows) and boxes per layer
+__host__ __device__ inline int rc_nbox(int E) { return (E + 255) / 256; }
+__host__ __device__ inline int rc_rows(int E) { return (E + rc_nbox(E) - 1) / rc_nbox(E); }
 
 struct StLayout {
-    int rt_max, rmax, dmax, rowb, dtileb;
-    size_t o_x, o_xt, o_rt, o_part, o_gu, o_dn, o_o, o_h, o_sel, total;
-    __host__ __device__ StLayout(int H, int E, int K, int I, int G) {
-        rt_max = (E + G - 1) / G;
+    int rmax, dmax, rowb, dtileb;
+    size_t rbs, rcb, o_x, o_xt, o_rc, o_xq, o_part, o_gu, o_dn, o_o, o_h, o_sel, total;
+    __host__ __device__ StLayout(int H, int E, int K, int I, int G, bool pg) {
         const int U = gu_unit(H), units = K * I / U;
         rmax = ((units + G - 1) / G) * U;
-        const int Ud = dn_unit(I), gq = H / Ud;
+        const int Ud = dq_unit(I), gq = H / Ud;
         dmax = ((gq + G - 1) / G) * Ud;
+        rbs = align_up((size_t)rc_rows(E) * dmax * sizeof(float), 128);  // one column box, 128-byte aligned
+        rcb = (size_t)rc_nbox(E) * rbs;
         rowb = (int)matrix_bytes(1, H);
         dtileb = (int)align_up(matrix_bytes(dmax, I), 16);
         o_x = kStHdr + kTabBytes;
         o_xt = o_x + (size_t)H * sizeof(float);
-        o_rt = o_xt + (size_t)H * sizeof(float);  // x again, lane-transposed for the gate/up lanes
-        o_part = o_rt + 2 * (size_t)rt_max * H * sizeof(float);  // two layers' router rows
+        o_rc = align_up(o_xt + (size_t)H * sizeof(float), 128);  // x again, lane-transposed for the gate/up lanes
+        // router columns [q0, q0 + dmax) of every row of one layer (and of the next, pre-gating)
+        o_xq = o_rc + (pg ? 2 : 1) * rcb;
+        o_part = o_xq + align_up((size_t)dmax * sizeof(float), 16);  // this CTA's slice of x
         o_gu = o_part + align_up((size_t)rmax * 4 * sizeof(float), 16);
         o_dn = o_gu + 2 * (size_t)rmax * rowb;
         o_o = o_dn + (size_t)K * dtileb;
@@ -83,15 +109,14 @@ struct StLayout {
 // This CTA's fixed share of every phase and its shared-memory layout, kept in shared memory
 // (read where needed) so that the layer loop keeps few registers live.
 struct StCta {
-    int e0, nr;              // router rows
     int p0, p1, ka, kb, n0, n1;  // gate/up (expert, row) pairs: two segments (experts ka, kb)
-    int q0, nq;              // down output rows
-    int rowb, dtileb, dmax;
-    uint32_t o_x, o_xt, o_rt, o_part, o_gu, o_dn, o_o, o_h, o_sel;
-    uint32_t rtb;            // bytes of one router buffer
+    int q0, nq;                  // down output rows = this CTA's slice of x
+    int rowb, dtileb, dmax, rbs, rcb;
+    uint32_t o_x, o_xt, o_rc, o_xq, o_part, o_gu, o_dn, o_o, o_h, o_sel;
 };
 
 struct StackArgs {
+    CUtensorMap wmap;        // the router weights as a [L * E][H] f32 matrix; box rc_rows x dmax
     float *x;
     float eps;
     const float *W;          // [L][E][H]
@@ -106,12 +131,20 @@ struct StackArgs {
     float *logits_out;  // [L][E] or NULL
     float *x_hist;      // [L][H] or NULL
     unsigned long long *ctr;
-    float *lg;   // [E]
-    float *lgp;  // [E] pre-gate logits: the next layer's router on this layer's input
-    float *h;    // [K][I]
+    long long *acc;     // [2][E] fixed-point router sums, by layer parity
+    long long *acc_pg;  // [2][E] the same for the pre-gate dots (next layer's router, this input)
+    float *h;           // [K][I]
     uint32_t *pg_hits;  // [L] or NULL
-    int layer0, nl, H, E, K, I, pregate;
+    int layer0, nl, H, E, K, I, pregate, n_layers;
 };
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
     unsigned long long v;
@@ -119,15 +152,34 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
     return v;
 }
 
+// *dst += p * 2^36 rounded to an integer (a reduction performed in L2).  Integer addition is
+// associative, so the sum does not depend on the order in which the CTAs arrive.
+__device__ __forceinline__ void red_fixed(long long *dst, float p, int32_t *ctrl) {
+    if (!(fabsf(p) < kFixMax)) {
+        dev_error(ctrl, RL_DEVERR_RANGE);
+        p = 0.f;
+    }
+    atomicAdd(reinterpret_cast<unsigned long long *>(dst), (unsigned long long)__float2ll_rn(p * kFixScale));
+}
+__device__ __forceinline__ float fixed_value(long long v) { return __ll2float_rn(v) * kFixInv; }
+
 // All CTAs of the grid meet; writes before it (through L2) are visible after it.  Thread 0
-// keeps the barrier target in a register; `target` = 0 means "not yet based".
+// keeps the barrier target in a register; `target` = 0 means "not yet based".  The arrival is a
+// release at GPU scope and the poll an acquire: together with the CTA barriers on both sides
+// they order every thread's writes before the meeting against every thread's reads after it.
+// Only the first arrival of a launch needs the counter's old value (to find the base); the
+// later ones are reductions that thread 0 does not wait for.
 __device__ __forceinline__ bool grid_sync(unsigned long long *ctr, unsigned long long &target, int *ok_s,
                                           int32_t *ctrl) {
-    __syncthreads();
+    cta_sync();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned long long old = atomicAdd(ctr, 1ull);
-        if (target == 0ull) target = old - old % gridDim.x + 1ull;  // +1 marks "based"
+        if (target == 0ull) {
+            unsigned long long old;
+            asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
+            target = old - old % gridDim.x + 1ull;  // +1 marks "based"
+        } else {
+            asm volatile("red.add.release.gpu.global.u64 [%0], 1;" ::"l"(ctr) : "memory");
+        }
         target += gridDim.x;
         bool ok = false;
         for (uint32_t i = 0; i < kSpinCap; ++i)
@@ -136,10 +188,9 @@ __device__ __forceinline__ bool grid_sync(unsigned long long *ctr, unsigned long
                 break;
             }
         if (!ok) dev_error(ctrl, RL_DEVERR_WAIT_TIMEOUT);
-        __threadfence();
         *ok_s = ok;
     }
-    __syncthreads();
+    cta_sync();  // also rejoins warp 0 after thread 0's wait
     return *ok_s != 0;
 }
 
@@ -148,13 +199,13 @@ __device__ __forceinline__ int gu_cut(const StCta &c, int U, int seg, int ch) {
     return ((seg == 0 ? c.n0 : c.n1) / U * ch / kStGuChunks) * U;
 }
 
-// NV = H / 128 float4 router columns per lane; GPL, SPLIT: gate/up lane geometry (moe_decode);
+// NV = H / 128 float4 columns per lane of x; GPL, SPLIT: gate/up lane geometry (moe_decode);
 // DGPL, LPR: down lane geometry.
 template <int NV, int GPL, int SPLIT, int DGPL, int LPR>
-__global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a) {
+__global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_constant__ StackArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *bar_rt = bars, *bar_dn = bars + 2, *bar_gu = bars + 3;  // bar_rt[2]: one per router buffer
+    uint64_t *bar_dn = bars, *bar_rc = bars + 1, *bar_gu = bars + 2;
     float *scale_s = reinterpret_cast<float *>(smem + 64);
     int *stop_s = reinterpret_cast<int *>(smem + 68);
     int *ok_s = reinterpret_cast<int *>(smem + 72);
@@ -166,12 +217,11 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
     constexpr int H = NV * 128;
     constexpr int U = H >= 2048 ? 1 : 2048 / H;  // gu_unit(H)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool pregate = a.pregate > 0;
 
     if (threadIdx.x == 0) {
         const int E = a.E, K = a.K, I = a.I, G = gridDim.x, b = blockIdx.x;
-        const StLayout lay(H, E, K, I, G);
-        C.e0 = (int)((long long)b * E / G);
-        C.nr = (int)((long long)(b + 1) * E / G) - C.e0;
+        const StLayout lay(H, E, K, I, G, pregate);
         const int units = K * I / U;
         C.p0 = (int)((long long)b * units / G) * U;
         C.p1 = (int)((long long)(b + 1) * units / G) * U;
@@ -180,15 +230,16 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
         C.kb = has ? (C.p1 - 1) / I : 0;
         C.n0 = has ? (C.ka == C.kb ? C.p1 : (C.ka + 1) * I) - C.p0 : 0;
         C.n1 = (C.p1 - C.p0) - C.n0;
-        const int Ud = dn_unit(I), gq = H / Ud;
-        C.q0 = (int)((long long)b * gq / G) * Ud;
-        C.nq = (int)((long long)(b + 1) * gq / G) * Ud - C.q0;
+        C.q0 = b * lay.dmax < H ? b * lay.dmax : H;
+        C.nq = H - C.q0 < lay.dmax ? H - C.q0 : lay.dmax;
         C.rowb = lay.rowb;
         C.dtileb = lay.dtileb;
         C.dmax = lay.dmax;
-        C.o_x = (uint32_t)lay.o_x; C.o_xt = (uint32_t)lay.o_xt; C.o_rt = (uint32_t)lay.o_rt; C.o_part = (uint32_t)lay.o_part;
-        C.o_gu = (uint32_t)lay.o_gu; C.o_dn = (uint32_t)lay.o_dn; C.o_o = (uint32_t)lay.o_o; C.o_h = (uint32_t)lay.o_h; C.o_sel = (uint32_t)lay.o_sel;
-        C.rtb = (uint32_t)((size_t)lay.rt_max * H * sizeof(float));
+        C.rbs = (int)lay.rbs;
+        C.rcb = (int)lay.rcb;
+        C.o_x = (uint32_t)lay.o_x; C.o_xt = (uint32_t)lay.o_xt; C.o_rc = (uint32_t)lay.o_rc; C.o_xq = (uint32_t)lay.o_xq;
+        C.o_part = (uint32_t)lay.o_part; C.o_gu = (uint32_t)lay.o_gu; C.o_dn = (uint32_t)lay.o_dn;
+        C.o_o = (uint32_t)lay.o_o; C.o_h = (uint32_t)lay.o_h; C.o_sel = (uint32_t)lay.o_sel;
         for (int i = 0; i < kStBars; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
     }
@@ -196,33 +247,83 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
     const int flag0 = ld_ctrl(a.ctrl);
     if (flag0 < a.layer0) return;  // an earlier layer already stopped the chain
 
-    // one thread: this CTA's router rows of layer index i (layer0 + i) into buffer i & 1.  The
-    // rows of layer i + 1 are in shared memory during layer i (they feed the pre-gate logits
-    // and then layer i + 1 itself); buffer b's n-th load completes phase n of bar_rt[b].
-    auto issue_router = [&](int i) {
-        const uint32_t bytes = (uint32_t)((size_t)C.nr * H * sizeof(float));
-        mbar_arrive_expect_tx(&bar_rt[i & 1], bytes);
-        bulk_g2s(smem + C.o_rt + (i & 1) * C.rtb, a.W + ((size_t)(a.layer0 + i) * a.E + C.e0) * H, bytes,
-                 &bar_rt[i & 1]);
+    const int E = a.E;
+    const int me = threadIdx.x;  // the router row (expert) whose columns this thread handles
+    constexpr int kColThread = kStProducer * 32 + 31;  // issues the router column copies
+    // Router columns [q0, q0 + dmax) of every row of layer index i (and of layer index i + 1
+    // for the pre-gate dots) into shared memory: tensor copies of rc_rows(E) x dmax floats
+    // (columns past H read as zeros), completion on bar_rc, whose n-th phase is layer index n.
+    // They depend on nothing computed, so they are requested a layer ahead.
+    auto issue_cols = [&](int i) {
+        const int nb = (pregate && i + 1 < a.nl) ? 2 : 1, nbox = rc_nbox(E), rows = rc_rows(E);
+        mbar_arrive_expect_tx(bar_rc, (uint32_t)(nb * C.rcb));
+        for (int q = 0; q < nb; ++q)
+            for (int k = 0; k < nbox; ++k)
+                tma_load_2d(smem + C.o_rc + (size_t)q * C.rcb + (size_t)k * C.rbs, &a.wmap,
+                            C.q0, (a.layer0 + i + q) * E + k * rows, bar_rc);
     };
-    const bool pregate = a.pregate > 0;
-    if (threadIdx.x == kStProducer * 32 && C.nr > 0) {
-        issue_router(0);
-        if (a.nl > 1) issue_router(1);
-    }
+    // This CTA's partial router dots of layer index i on its slice of x_{layer0 + i} (in the
+    // shared xq slice), sequential in the column order, added into acc[i & 1]; pre-gating, the
+    // next layer's dots into acc_pg[i & 1].  The columns have landed (bar_rc, waited by the caller).
+    auto add_partials = [&](int i) {
+        const int nq = C.nq;
+        if (me < E && nq > 0) {
+            const float4 *xq = reinterpret_cast<const float4 *>(smem + C.o_xq);
+            const int rows = rc_rows(E);
+            const float4 *wr = reinterpret_cast<const float4 *>(smem + C.o_rc + (size_t)(me / rows) * C.rbs) +
+                               (size_t)(me % rows) * (C.dmax / 4);
+            const int n4 = nq / 4;
+            float p = 0.f;
+            for (int c = 0; c < n4; ++c) {
+                const float4 w = wr[c], v = xq[c];
+                p = fmaf(w.x, v.x, p); p = fmaf(w.y, v.y, p); p = fmaf(w.z, v.z, p); p = fmaf(w.w, v.w, p);
+            }
+            red_fixed(a.acc + (size_t)(i & 1) * E + me, p, a.ctrl);
+            if (pregate && i + 1 < a.nl) {
+                wr += C.rcb / sizeof(float4);
+                float q = 0.f;
+                for (int c = 0; c < n4; ++c) {
+                    const float4 w = wr[c], v = xq[c];
+                    q = fmaf(w.x, v.x, q); q = fmaf(w.y, v.y, q); q = fmaf(w.z, v.z, q); q = fmaf(w.w, v.w, q);
+                }
+                red_fixed(a.acc_pg + (size_t)(i & 1) * E + me, q, a.ctrl);
+            }
+        }
+    };
 
     unsigned long long target = 0;  // grid barrier state (thread 0)
-    // copies in flight, for the exit path: the layer index of the last router load of each
-    // buffer (-1: none) and whether this layer's expert copies were issued
-    int rt_last[2] = {C.nr > 0 ? 0 : -1, (C.nr > 0 && a.nl > 1) ? 1 : -1};
-    bool ex_issued = false;
+    bool ex_issued = false;         // this layer's expert copies are in flight
+    int rc_pend = -1;               // layer index whose router columns are in flight (-1: none)
     bool failed = false;
+    // ---- prologue: the accumulators start from zero (CTA 0 clears them; a grid barrier orders
+    // the clear before any CTA's sums), then every CTA adds the dots of its slice of x_{layer0}
+    if (C.nq > 0) {
+        if (threadIdx.x == kColThread) issue_cols(0);
+        rc_pend = 0;
+    }
+    if (blockIdx.x == 0)
+        for (int j = threadIdx.x; j < 2 * E; j += kStThreads) {
+            __stcg(a.acc + j, 0ll);
+            __stcg(a.acc_pg + j, 0ll);
+        }
+    if ((int)threadIdx.x < C.nq) reinterpret_cast<float *>(smem + C.o_xq)[threadIdx.x] = __ldcg(a.x + C.q0 + threadIdx.x);
+    if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) failed = true;
+    if (!failed) {
+        if (warp == 0 && C.nq > 0 && !mbar_spin_warp(bar_rc, 0u)) failed = true;
+        failed = cta_sync_or(failed) != 0;
+    }
+    if (!failed) {
+        rc_pend = -1;
+        add_partials(0);
+        if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) failed = true;
+    }
     uint32_t ph = 0;
-    for (int i = 0; i < a.nl; ++i, ph ^= 1u) {
+    for (int i = 0; !failed && i < a.nl; ++i, ph ^= 1u) {
         const int l = a.layer0 + i;
         const bool last = i + 1 == a.nl;
         ex_issued = false;
-        // ---------------- A: x_l, its scale, this CTA's logits ----------------
+        // ---------------- B: x_l, its scale, the logits, the selection (the same in every CTA) ----------------
+        const long long accv = me < E ? __ldcg(a.acc + (size_t)(i & 1) * E + me) : 0ll;
         {
             float *x_s = reinterpret_cast<float *>(smem + C.o_x);
             float4 *xt_s = reinterpret_cast<float4 *>(smem + C.o_xt);
@@ -234,65 +335,34 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
                 const int hf = H / 4 / SPLIT, h = j / hf, r = j % hf, L = r / (2 * GPL), q = r % (2 * GPL);
                 xt_s[(h * 2 * GPL + q) * 32 + L] = v;
             }
-            __syncthreads();
+            cta_sync();
             if (warp == 0) {
                 const float r = a.eps >= 0.f ? rms_scale_warp(x_s, H, a.eps) : 1.f;
                 if (lane == 0) *scale_s = r;
             }
             if (a.x_hist && blockIdx.x == 0)
                 for (int j = threadIdx.x; j < H; j += kStThreads) a.x_hist[(size_t)l * H + j] = x_s[j];
-            const int nr = C.nr;
-            const bool pg = pregate && !last;
-            if (warp < nr && !mbar_wait_warp(&bar_rt[i & 1], (i >> 1) & 1)) failed = true;
-            if (pg && warp < nr && !mbar_wait_warp(&bar_rt[(i + 1) & 1], ((i + 1) >> 1) & 1)) failed = true;
-            __syncthreads();
-            if (warp < nr && !failed) {
-                const float4 *xr = reinterpret_cast<const float4 *>(x_s);
-                const bool norm = a.eps >= 0.f;
-                const float r = *scale_s;
-                // this layer's logit of row e0 + warp, then (pre-gating) the next layer's
-#pragma unroll 1
-                for (int q = 0; q < (pg ? 2 : 1); ++q) {
-                    const float4 *wr = reinterpret_cast<const float4 *>(smem + C.o_rt + ((i + q) & 1) * C.rtb) +
-                                       (size_t)warp * (H / 4);
-                    unsigned long long a0 = 0, a1 = 0;
-#pragma unroll
-                    for (int j = 0; j < NV; ++j) {
-                        float4 v = xr[lane + 32 * j];
-                        if (norm) { v.x *= r; v.y *= r; v.z *= r; v.w *= r; }
-                        const float4 w = wr[lane + 32 * j];
-                        a0 = ffma2(pack2(__float_as_uint(w.x), __float_as_uint(w.y)),
-                                   pack2(__float_as_uint(v.x), __float_as_uint(v.y)), a0);
-                        a1 = ffma2(pack2(__float_as_uint(w.z), __float_as_uint(w.w)),
-                                   pack2(__float_as_uint(v.z), __float_as_uint(v.w)), a1);
-                    }
-                    const float s = warp_sum(hsum2(a0) + hsum2(a1));
-                    if (lane == 0) {
-                        const int e = C.e0 + warp;
-                        const float lv = s + (a.bias ? a.bias[(size_t)(l + q) * a.E + e] : 0.f);
-                        if (q == 0) {
-                            __stcg(a.lg + e, lv);
-                            if (a.logits_out) a.logits_out[(size_t)l * a.E + e] = lv;
-                        } else {
-                            __stcg(a.lgp + e, lv);
-                        }
-                    }
-                }
-            }
+            // acc_pg[(i + 1) & 1] was last read in D of the previous layer; it takes this
+            // layer's pre-gate sums next
+            if (pregate && i > 0 && blockIdx.x == 0)
+                for (int j = threadIdx.x; j < E; j += kStThreads) __stcg(a.acc_pg + (size_t)((i + 1) & 1) * E + j, 0ll);
+            cta_sync();
         }
-        failed = __syncthreads_or(failed) != 0;
-        if (failed) break;
-        if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
-
-        // ---------------- B: selection (the same in every CTA), expert copies ----------------
         {
             const int K = a.K;
+            // logit = rs * (W x) + bias: the RMSNorm scale applied to the summed dots
+            uint32_t key = 0u;
+            if (me < E) {
+                const float lv = fmaf(fixed_value(accv), *scale_s, a.bias ? a.bias[(size_t)l * E + me] : 0.f);
+                key = order_key(lv);
+                if (a.logits_out && blockIdx.x == 0) a.logits_out[(size_t)l * E + me] = lv;
+            }
             int my_id;
             float my_val;
             uint64_t slot;
             {
                 uint8_t *sb = smem + C.o_sel;
-                cta_topk_thr<kStSelWarps>(a.lg, a.table + (size_t)l * a.E, a.E, K, reinterpret_cast<uint32_t *>(sb),
+                cta_topk_thr<kStSelWarps>(key, a.table + (size_t)l * E, E, K, reinterpret_cast<uint32_t *>(sb),
                                           reinterpret_cast<int *>(sb + 2048), reinterpret_cast<uint64_t *>(sb + 4096),
                                           reinterpret_cast<uint32_t *>(sb + 8192), reinterpret_cast<int *>(sb + 8256),
                                           reinterpret_cast<int *>(sb + 8320), my_id, my_val, slot);
@@ -328,7 +398,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
                 if (lane == 0) *stop_s = stop;
             }
         }
-        __syncthreads();
+        cta_sync();
         if (*stop_s) break;
         // the last warp issues the gate/up copies, the one before it the down copies (two
         // issuing warps halve the issue time)
@@ -352,6 +422,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
                     bulk_g2s(gdst + (size_t)n * rowb, base + matb + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
                 }
             }
+            // then the next layer's router columns, behind the expert copies
+            if (threadIdx.x == kColThread && !last && C.nq > 0) issue_cols(i + 1);
         } else if (warp == kStProducer - 1) {
             fence_proxy_async_smem();
             const int K = a.K, I = a.I;
@@ -370,8 +442,9 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
         }
         // the computing warps start once every copy is issued: issued under their load the
         // copies take about three times longer
-        __syncthreads();
+        cta_sync();
         ex_issued = true;
+        if (!last && C.nq > 0) rc_pend = i + 1;
 
         // ---------------- C: gate/up + SwiGLU of this CTA's pairs ----------------
         if (C.p1 > C.p0) {
@@ -430,40 +503,40 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
                         part[((q - p0) * 2 + half) * 2 + 1] = uv2;
                     }
                 }
+                __syncwarp();  // rejoin before the next row's shuffles (see cta_sync)
             }
             if (to) failed = true;
         }
-        failed = __syncthreads_or(failed) != 0;
+        failed = cta_sync_or(failed) != 0;
         if (failed) break;
         {
             const int p0 = C.p0, np = C.p1 - C.p0;
             const float *part = reinterpret_cast<const float *>(smem + C.o_part);
             for (int t = threadIdx.x; t < np; t += kStThreads) __stcg(a.h + p0 + t, swiglu_part<SPLIT>(part + 4 * t));
         }
-        // buffer i & 1 (free since phase A) takes the rows of layer i + 2; issued after this
-        // layer's expert copies so that it never delays them
-        if (C.nr > 0 && i + 2 < a.nl) {
-            if (threadIdx.x == kStProducer * 32) {
-                fence_proxy_async_smem();
-                issue_router(i + 2);
-            }
-            rt_last[i & 1] = i + 2;
-        }
         if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
 
         // ---------------- D: down rows of every expert, ordered combine, residual ----------------
+        // acc[i & 1] was read by every CTA in B; it takes the sums of layer index i + 2 next
+        if (blockIdx.x == 0)
+            for (int j = threadIdx.x; j < E; j += kStThreads) __stcg(a.acc + (size_t)(i & 1) * E + j, 0ll);
         // The producer warp (idle in D when K > 8) meanwhile selects the pre-gated prediction of
         // the next layer's experts and prefetches this CTA's slice of their records into L2
         // ("Red Lite dev23", "What changed": pre-gated expert prefetch).
         if (pregate && !last && warp == kStProducer) {
             const int P = a.pregate;
+            const float rs = *scale_s;
+            const long long *ap = a.acc_pg + (size_t)(i & 1) * E;
+            const float *b1 = a.bias ? a.bias + (size_t)(l + 1) * E : nullptr;
             int pid;
             float pval;
-            warp_topk<kStCand>(a.lgp, a.E, P, pid, pval);
+            warp_topk_by<kStCand, kStPredMax>(
+                [&](int e) { return e < E ? order_key(fmaf(fixed_value(__ldcg(ap + e)), rs, b1 ? b1[e] : 0.f)) : 0u; },
+                P, pid, pval);
             uint64_t pslot = 0;
             if (lane < P) {
                 pred_s[lane] = pid;
-                pslot = __ldcg(a.table + (size_t)(l + 1) * a.E + pid);
+                pslot = __ldcg(a.table + (size_t)(l + 1) * E + pid);
             }
             const size_t rec = 3 * matrix_bytes(a.I, H);
             const size_t total = (size_t)P * rec;
@@ -484,14 +557,14 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
             // h of all K experts into shared memory, once per CTA, lane-transposed: the q-th
             // float4 of lane sl of a row group sits at [k][q][sl], so a group's loads do not
             // collide on banks
-            {
+            if (nq > 0) {
                 const int I = a.I, f4 = I / 4;
                 float4 *h_s = reinterpret_cast<float4 *>(smem + C.o_h);
                 for (int d = threadIdx.x; d < K * f4; d += kStThreads) {
                     const int k = d / f4, r = d % f4, q = r / LPR, sl = r % LPR;
                     h_s[d] = __ldcg(reinterpret_cast<const float4 *>(a.h) + k * f4 + sl * (2 * DGPL) + q);
                 }
-                __syncthreads();
+                cta_sync();
             }
             if (nq > 0) {
                 constexpr int kNG = kStThreads / LPR;  // lane groups in the CTA
@@ -518,11 +591,12 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
                         const bool real = rr < nq;
                         const float o = down_row<DGPL, LPR>(tile, real ? rr : 0, I, sl, hv, tabc);
                         if (real && sl == 0) o_s[k * dmax + rr] = o;
+                        __syncwarp();
                     }
                 }
             }
         }
-        failed = __syncthreads_or(failed) != 0;
+        failed = cta_sync_or(failed) != 0;
         if (failed) break;
         ex_issued = false;
         if ((int)threadIdx.x < C.nq) {
@@ -530,14 +604,22 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
             const float *o_s = reinterpret_cast<const float *>(smem + C.o_o);
             const float *x_s = reinterpret_cast<const float *>(smem + C.o_x);
             const float acc = ordered_combine(w_s, o_s + threadIdx.x, C.dmax, a.K);
-            __stcg(a.x + r, x_s[r] + acc);
+            const float xv = x_s[r] + acc;
+            __stcg(a.x + r, xv);
+            reinterpret_cast<float *>(smem + C.o_xq)[threadIdx.x] = xv;
         }
-        if (!last && !grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
+        if (last) break;
+        // the next layer's router dots on this CTA's slice of x_{l+1}
+        if (warp == 0 && C.nq > 0 && !mbar_spin_warp(bar_rc, (uint32_t)((i + 1) & 1))) failed = true;
+        failed = cta_sync_or(failed) != 0;
+        if (failed) break;
+        rc_pend = -1;
+        add_partials(i + 1);
+        if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
     }
     // ---- exit: no copy into this CTA's shared memory may still be in flight ----
     if (threadIdx.x == 0) {
-        for (int b = 0; b < 2; ++b)
-            if (rt_last[b] >= 0) mbar_wait(&bar_rt[b], (uint32_t)((rt_last[b] >> 1) & 1));
+        if (rc_pend >= 0) mbar_wait(bar_rc, (uint32_t)(rc_pend & 1));
         if (ex_issued) {
             if (C.nq > 0) mbar_wait(bar_dn, ph);
             for (int bi = 0; bi < 2 * kStGuChunks; ++bi) {
@@ -546,18 +628,45 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const StackArgs a)
             }
         }
     }
-    __syncthreads();
+    cta_sync();
+}
+
+// cuTensorMapEncodeTiled, from the driver through the runtime (no link to the driver library)
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
 }
 
 template <int NV, int GPL, int SPLIT, int DGPL, int LPR>
-static rl_status launch_stack(const StackArgs &a, cudaStream_t s) {
+static rl_status launch_stack(StackArgs a, cudaStream_t s) {
     auto kern = stack_kernel<NV, GPL, SPLIT, DGPL, LPR>;
     const int G = sm_count();
-    const StLayout lay(a.H, a.E, a.K, a.I, G);
-    if (lay.total > 227 * 1024 || lay.rt_max > kStWarps || lay.rmax > a.I || lay.dmax > kStThreads ||
+    const StLayout lay(a.H, a.E, a.K, a.I, G, a.pregate > 0);
+    if (lay.total > 227 * 1024 || a.E > kStThreads || G > kStMaxGrid || lay.rmax > a.I || lay.dmax > 256 ||
         kStWarps / a.K < 1)
         return fail(RL_ERR_UNSUPPORTED, "moe_decode_stack: shape does not fit one CTA per SM (H=%d E=%d K=%d I=%d)",
                     a.H, a.E, a.K, a.I);
+    // the router as a [n_layers * E][H] f32 matrix; a box is rc_rows(E) rows x dmax columns
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+    if (!enc) return fail(RL_ERR_CUDA, "moe_decode_stack: cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t gdim[2] = {(cuuint64_t)a.H, (cuuint64_t)a.n_layers * a.E};
+    const cuuint64_t gstride[1] = {(cuuint64_t)a.H * sizeof(float)};
+    const cuuint32_t box[2] = {(cuuint32_t)lay.dmax, (cuuint32_t)rc_rows(a.E)};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult cr = enc(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(a.W), gdim, gstride, box,
+                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS)
+        return fail(RL_ERR_UNSUPPORTED, "moe_decode_stack: router tensor map rejected (error %d, box %d x %d)", (int)cr,
+                    lay.dmax, rc_rows(a.E));
     rl_status st = allow_smem((const void *)kern, lay.total);
     if (st != RL_OK) return st;
     int occ = 0;
@@ -596,7 +705,7 @@ using namespace rl;
 
 extern "C" size_t moe_decode_stack_workspace_bytes(const rl_moe_shape *shp) {
     if (!shp || shp->n_experts <= 0 || shp->top_k <= 0 || shp->inter <= 0) return 0;
-    return 256 + 2 * align_up((size_t)shp->n_experts * sizeof(float), 256) +
+    return 256 + 2 * align_up(2 * (size_t)shp->n_experts * sizeof(long long), 256) +
            align_up((size_t)shp->top_k * shp->inter * sizeof(float), 256);
 }
 
@@ -622,7 +731,7 @@ extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, i
     if (pregate < 0 || pregate > kStPredMax || pregate > shp->n_experts)
         return fail(RL_ERR_INVALID, "moe_decode_stack: pregate %d outside [0, min(%d, n_experts)]", pregate, kStPredMax);
     if (n_layers == 0) return RL_OK;
-    StackArgs a;
+    StackArgs a = {};
     a.x = x;
     a.eps = norm_eps;
     a.W = w_router;
@@ -638,14 +747,15 @@ extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, i
     a.x_hist = x_hist;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     a.ctr = reinterpret_cast<unsigned long long *>(w8);
-    const size_t lgb = align_up((size_t)shp->n_experts * sizeof(float), 256);
-    a.lg = reinterpret_cast<float *>(w8 + 256);
-    a.lgp = reinterpret_cast<float *>(w8 + 256 + lgb);
-    a.h = reinterpret_cast<float *>(w8 + 256 + 2 * lgb);
+    const size_t accb = align_up(2 * (size_t)shp->n_experts * sizeof(long long), 256);
+    a.acc = reinterpret_cast<long long *>(w8 + 256);
+    a.acc_pg = reinterpret_cast<long long *>(w8 + 256 + accb);
+    a.h = reinterpret_cast<float *>(w8 + 256 + 2 * accb);
     a.pg_hits = pregate_hits;
     a.pregate = pregate;
     a.layer0 = layer0;
     a.nl = n_layers;
+    a.n_layers = shp->n_layers;
     a.H = shp->hidden;
     a.E = shp->n_experts;
     a.K = shp->top_k;

@@ -215,10 +215,15 @@ def _bits(t):
     return t.view(torch.int32) if t.dtype == torch.float32 else t
 
 
-def test_decode_stack_fused_equals_chain(stack_model):
+def test_decode_stack_fused_vs_chain(stack_model):
     """moe_decode_stack (one launch per token for all 48 layers) against the per-layer chain
-    rl_route + moe_decode: logits, ids, weights, slots, every layer's input and the token's
-    output are bit-identical; the fused layers also match the oracle."""
+    rl_route + moe_decode.  The fused launch sums every router row across its CTAs in 64-bit
+    fixed point, so its logits differ from rl_route's f32 dots in the last bits only: at the
+    first layer (same input) within 1e-6 of the row scale; the selections equal except at a
+    genuine near tie (where the two paths part); the token outputs within the f32 bound.  Every
+    fused layer of the first token, and every 4th of the others, matches the oracle from its
+    own input.  The pre-gated prefetch changes no result: with and without it the fused runs
+    are bit-identical, and its hit counts follow from the GPU's own layer inputs."""
     engine = _engine()
     w, m, o = stack_model
     toks = [0, 77, w.tokens - 1]
@@ -240,13 +245,30 @@ def test_decode_stack_fused_equals_chain(stack_model):
             torch.cuda.synchronize()
             res.append([_bits(v) for v in (b.logits, b.ids, b.weights, b.slots, y)])
         assert b.ctrl.tolist() == [0x7FFFFFFF, 0] and int(b.miss.sum()) == 0
-        outs[mode] = (res, _bits(hist), hist.double().cpu().numpy(), res[0][4].view(torch.float32).double().numpy())
-    for other in ("fused", "fused_pregate"):   # the prefetch never changes a result
-        for ra, rb in zip(outs["chain"][0], outs[other][0]):
-            for name, a_, b_ in zip(("logits", "ids", "weights", "slots", "y"), ra, rb):
-                assert torch.equal(a_, b_), (other, name)
-        assert torch.equal(outs["chain"][1], outs[other][1])
-    # pre-gate hits: layer l's experts found in the top-32 of router l+1... applied at layer l-1,
+        outs[mode] = (res, _bits(hist), hist.double().cpu().numpy())
+    # the prefetch never changes a result
+    for ra, rb in zip(outs["fused"][0], outs["fused_pregate"][0]):
+        for name, a_, b_ in zip(("logits", "ids", "weights", "slots", "y"), ra, rb):
+            assert torch.equal(a_, b_), name
+    assert torch.equal(outs["fused"][1], outs["fused_pregate"][1])
+    # fused against chain
+    for i in range(len(toks)):
+        rc, rf = outs["chain"][0][i], outs["fused"][0][i]
+        lc, lf = rc[0].view(torch.float32).double().numpy(), rf[0].view(torch.float32).double().numpy()
+        assert np.max(np.abs(lc[0] - lf[0])) <= 1e-6 * np.max(np.abs(lc[0])), i
+        ic, if_ = rc[1].numpy(), rf[1].numpy()
+        diff = np.nonzero(np.any(ic != if_, axis=1))[0]
+        if len(diff):   # only a genuine near tie may differ; the paths part there
+            l = int(diff[0])
+            for a_, b_ in zip(ic[l], if_[l]):
+                if a_ != b_:
+                    assert abs(lc[l][a_] - lc[l][b_]) <= 1e-5 * np.max(np.abs(lc[l])), (i, l)
+            print(f"token {toks[i]}: near tie at layer {l}")
+            continue
+        assert torch.equal(rc[3], rf[3]), i
+        yc, yf = rc[4].view(torch.float32).double().numpy(), rf[4].view(torch.float32).double().numpy()
+        assert rel_l2(yf, yc) <= REL_F32, (i, rel_l2(yf, yc))
+    # pre-gate hits: layer l's experts found in the top-32 of router l applied at layer l-1,
     # recomputed on the host from the GPU's own layer inputs (f32 logits; near ties may move one)
     Hh = outs["fused_pregate"][2]
     hits = hits.cpu().numpy()
@@ -261,20 +283,23 @@ def test_decode_stack_fused_equals_chain(stack_model):
     rate = hits[:, 1:].mean() / w.top_k
     print(f"pre-gate (top-32) hit rate {rate:.2f}")
     assert rate > 0.5
-    # the fused run of token 0 against the oracle, every 4th layer from its own layer inputs
-    H = outs["fused"][2][0]
-    y_last = outs["fused"][3]
+    # the fused layers against the oracle, each from its own layer input
     rep = {}
-    for l in range(0, m.L, 4):
-        xn = oracle.rmsnorm(H[l:l + 1])
-        lg = outs["fused"][0][0][0].view(torch.float32).numpy()[l:l + 1]
-        ids = outs["fused"][0][0][1].numpy()[l:l + 1]
-        wts = outs["fused"][0][0][2].view(torch.float32).numpy()[l:l + 1]
-        sl = outs["fused"][0][0][3].numpy().view(np.uint64)[l:l + 1]
-        r = check_route(lg, ids, wts, sl, oracle.router_logits(xn, o.router(l)), o.table_row(l), w.top_k, l, rep)
-        y_o = o.experts(xn, r.ids, r.weights, r.slots)
-        x_next = H[l + 1] if l + 1 < m.L else y_last
-        assert rel_l2(x_next - H[l], y_o[0]) <= REL_F32, l
+    for i in range(len(toks)):
+        H = outs["fused"][2][i]
+        y_last = outs["fused"][0][i][4].view(torch.float32).double().numpy()
+        r_all = outs["fused"][0][i]
+        for l in range(0, m.L, 1 if i == 0 else 4):
+            xn = oracle.rmsnorm(H[l:l + 1])
+            lg = r_all[0].view(torch.float32).numpy()[l:l + 1]
+            ids = r_all[1].numpy()[l:l + 1]
+            wts = r_all[2].view(torch.float32).numpy()[l:l + 1]
+            sl = r_all[3].numpy().view(np.uint64)[l:l + 1]
+            r = check_route(lg, ids, wts, sl, oracle.router_logits(xn, o.router(l)), o.table_row(l), w.top_k, l, rep)
+            y_o = o.experts(xn, r.ids, r.weights, r.slots)
+            x_next = H[l + 1] if l + 1 < m.L else y_last
+            assert rel_l2(x_next - H[l], y_o[0]) <= REL_F32, (i, l)
+    print(f"fused stack: near ties {rep.get('near_ties', 0)}")
 
 
 def test_decode_stack_bounded_residency():

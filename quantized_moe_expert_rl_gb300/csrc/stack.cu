@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     uint4 *tab = reinterpret_cast<uint4 *>(smem + kStHdr);
     constexpr int H = NV * 128;
     constexpr int U = H >= 2048 ? 1 : 2048 / H;  // gu_unit(H)
+    static_assert(2 * DGPL <= LPR, "the h staging swizzle sl ^ q needs q < LPR");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool pregate = a.pregate > 0;
 
@@ -263,8 +264,11 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                             C.q0, (a.layer0 + i + q) * E + k * rows, bar_rc);
     };
     // This CTA's partial router dots of layer index i on its slice of x_{layer0 + i} (in the
-    // shared xq slice), sequential in the column order, added into acc[i & 1]; pre-gating, the
-    // next layer's dots into acc_pg[i & 1].  The columns have landed (bar_rc, waited by the caller).
+    // shared xq slice), added into acc[i & 1]; pre-gating, the next layer's dots into
+    // acc_pg[i & 1].  The columns have landed (bar_rc, waited by the caller).  Each dot runs
+    // over the float4 chunks of its row starting at chunk (me / 2) mod (nq / 4): rows are 16 *
+    // nq bytes apart, so 8 consecutive rows read in step would share banks; the rotation (a
+    // fixed order per row) spreads them.
     auto add_partials = [&](int i) {
         const int nq = C.nq;
         if (me < E && nq > 0) {
@@ -272,9 +276,10 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             const int rows = rc_rows(E);
             const float4 *wr = reinterpret_cast<const float4 *>(smem + C.o_rc + (size_t)(me / rows) * C.rbs) +
                                (size_t)(me % rows) * (C.dmax / 4);
-            const int n4 = nq / 4;
+            const int n4 = nq / 4, rot = (me >> 1) % n4;
             float p = 0.f;
-            for (int c = 0; c < n4; ++c) {
+            for (int j = 0; j < n4; ++j) {
+                const int c = j + rot < n4 ? j + rot : j + rot - n4;
                 const float4 w = wr[c], v = xq[c];
                 p = fmaf(w.x, v.x, p); p = fmaf(w.y, v.y, p); p = fmaf(w.z, v.z, p); p = fmaf(w.w, v.w, p);
             }
@@ -282,7 +287,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             if (pregate && i + 1 < a.nl) {
                 wr += C.rcb / sizeof(float4);
                 float q = 0.f;
-                for (int c = 0; c < n4; ++c) {
+                for (int j = 0; j < n4; ++j) {
+                    const int c = j + rot < n4 ? j + rot : j + rot - n4;
                     const float4 w = wr[c], v = xq[c];
                     q = fmaf(w.x, v.x, q); q = fmaf(w.y, v.y, q); q = fmaf(w.z, v.z, q); q = fmaf(w.w, v.w, q);
                 }
@@ -328,12 +334,13 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             float *x_s = reinterpret_cast<float *>(smem + C.o_x);
             float4 *xt_s = reinterpret_cast<float4 *>(smem + C.o_xt);
             // x_s in order; xt_s lane-transposed for the gate/up lanes: float4 q of the slice of
-            // lane L of row half h (columns h H/SPLIT + L 8 GPL ...) sits at [h][q][L]
+            // lane L of row half h (columns h H/SPLIT + L 8 GPL ...) sits at [h][q][L ^ q] (the
+            // xor spreads the staging writes of consecutive q over the banks)
             for (int j = threadIdx.x; j < H / 4; j += kStThreads) {
                 const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.x) + j);
                 reinterpret_cast<float4 *>(x_s)[j] = v;
                 const int hf = H / 4 / SPLIT, h = j / hf, r = j % hf, L = r / (2 * GPL), q = r % (2 * GPL);
-                xt_s[(h * 2 * GPL + q) * 32 + L] = v;
+                xt_s[(h * 2 * GPL + q) * 32 + (L ^ q)] = v;
             }
             cta_sync();
             if (warp == 0) {
@@ -460,7 +467,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 const float4 *xt_s = reinterpret_cast<const float4 *>(smem + C.o_xt);
 #pragma unroll
                 for (int q = 0; q < 2 * GPL; ++q) {
-                    const float4 v = xt_s[(half * 2 * GPL + q) * 32 + lane];
+                    const float4 v = xt_s[(half * 2 * GPL + q) * 32 + (lane ^ q)];
                     xv[4 * q] = v.x * r; xv[4 * q + 1] = v.y * r; xv[4 * q + 2] = v.z * r; xv[4 * q + 3] = v.w * r;
                 }
             }
@@ -554,15 +561,18 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             // (K)-th of its rows; a warp runs as many passes as its busier half needs, so the
             // shuffles of a row's reduction always see the whole warp
             const int nq = C.nq, K = a.K;
-            // h of all K experts into shared memory, once per CTA, lane-transposed: the q-th
-            // float4 of lane sl of a row group sits at [k][q][sl], so a group's loads do not
-            // collide on banks
+            // h of all K experts into shared memory, once per CTA, lane-transposed: float4 q of
+            // lane sl of a row group (h_k[8 DGPL sl + 4 q ...]) sits at [k][q][sl ^ q], so that a
+            // group's reads (fixed q, 16 or 32 consecutive sl) and the staging writes (8
+            // consecutive q of one sl per quarter warp) both spread over all banks.  The global
+            // reads are coalesced.
             if (nq > 0) {
                 const int I = a.I, f4 = I / 4;
                 float4 *h_s = reinterpret_cast<float4 *>(smem + C.o_h);
+                const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
                 for (int d = threadIdx.x; d < K * f4; d += kStThreads) {
-                    const int k = d / f4, r = d % f4, q = r / LPR, sl = r % LPR;
-                    h_s[d] = __ldcg(reinterpret_cast<const float4 *>(a.h) + k * f4 + sl * (2 * DGPL) + q);
+                    const int k = d / f4, r = d % f4, sl = r / (2 * DGPL), q = r % (2 * DGPL);
+                    h_s[k * f4 + q * LPR + (sl ^ q)] = __ldcg(h4 + d);
                 }
                 cta_sync();
             }
@@ -577,7 +587,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 const float4 *h_s = reinterpret_cast<const float4 *>(smem + C.o_h) + (size_t)k * (I / 4);
 #pragma unroll
                 for (int q = 0; q < 2 * DGPL; ++q) {
-                    const float4 v = h_s[q * LPR + sl];
+                    const float4 v = h_s[q * LPR + (sl ^ q)];
                     hv[4 * q] = v.x; hv[4 * q + 1] = v.y; hv[4 * q + 2] = v.z; hv[4 * q + 3] = v.w;
                 }
                 if (trips > 0 && !mbar_wait_warp(bar_dn, ph)) {

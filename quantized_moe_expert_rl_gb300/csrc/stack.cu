@@ -429,8 +429,13 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     bulk_g2s(gdst + (size_t)n * rowb, base + matb + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
                 }
             }
-            // then the next layer's router columns, behind the expert copies
-            if (threadIdx.x == kColThread && !last && C.nq > 0) issue_cols(i + 1);
+            if (threadIdx.x == kColThread && !last) {
+                // then the next layer's router columns, behind the expert copies, and its
+                // residency row into L2 (read once per token, it would come from HBM)
+                if (C.nq > 0) issue_cols(i + 1);
+                if ((E & 1) == 0 && (reinterpret_cast<uintptr_t>(a.table) & 15) == 0)  // 16-byte pieces
+                    prefetch_l2_bulk(a.table + (size_t)(l + 1) * E, (uint32_t)(E * sizeof(uint64_t)));
+            }
         } else if (warp == kStProducer - 1) {
             fence_proxy_async_smem();
             const int K = a.K, I = a.I;

@@ -196,8 +196,10 @@ def enqueue_decode_token_fused(model: Model, b: DecodeBuffers, x_in: torch.Tenso
                                layer0: int = 0, pregate: int = 0,
                                pregate_hits: torch.Tensor | None = None) -> None:
     """Stacked decode of one token, layers [layer0, L), in ONE launch (moe_decode_stack):
-    y_out = x_in, then per layer y_out += MoE(RMSNorm(y_out)).  Bit-identical to
-    enqueue_decode_token(stacked=True).  x_hist[l] (optional) receives layer l's input.
+    y_out = x_in, then per layer y_out += MoE(RMSNorm(y_out)).  The expert, RMSNorm and
+    selection arithmetic is that of enqueue_decode_token(stacked=True); the router logits are
+    summed across the launch's CTAs in 64-bit fixed point, so they agree with rl_route's to the
+    last bits.  x_hist[l] (optional) receives layer l's input.
     pregate > 0 prefetches into L2 the next layer's predicted experts (never changes results);
     pregate_hits[l] (optional) receives how many of layer l's experts were predicted."""
     y_out.copy_(x_in)

@@ -339,3 +339,24 @@ def test_decode_stack_bounded_residency():
         n_early += len(st.early_outs)
     print(f"bounded fused decode: {n_early} early-outs over {base.tokens} tokens")
     assert n_early > 0
+
+
+def test_decode_stack_range_flag():
+    """A residual stream far outside the fixed-point range of the fused kernel's router sums
+    (|partial dot| >= 2^19) raises RL_DEVERR_RANGE in ctrl[1] and the launch still completes;
+    an input of ordinary scale leaves ctrl[1] at 0."""
+    engine = _engine()
+    from quantized_moe_expert_rl_gb300 import _lib
+    w = replace(synth.WORKLOADS["tiny"], n_layers=3)
+    m = engine.Model(w)
+    b = engine.DecodeBuffers.make(m)
+    x = torch.from_numpy(synth.tokens(w, 0, 1)).cuda()[0]
+    y = torch.zeros(w.hidden, device="cuda")
+    engine.enqueue_decode_token_fused(m, b, x, y)
+    torch.cuda.synchronize()
+    assert b.ctrl.tolist() == [0x7FFFFFFF, 0]
+    b.ctrl.copy_(torch.tensor([0x7FFFFFFF, 0], dtype=torch.int32))
+    engine.enqueue_decode_token_fused(m, b, x * 1e9, y)
+    torch.cuda.synchronize()
+    c = b.ctrl.tolist()
+    assert c[1] & _lib.RL_DEVERR_RANGE and not (c[1] & _lib.RL_DEVERR_WAIT_TIMEOUT), c

@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     float *scale_s = reinterpret_cast<float *>(smem + 64);
     int *stop_s = reinterpret_cast<int *>(smem + 68);
     int *ok_s = reinterpret_cast<int *>(smem + 72);
+    int *iss_s = reinterpret_cast<int *>(smem + 76);  // copies issued at the end of C: bit 0 down rows, bit 1 router columns
     StCta &C = *reinterpret_cast<StCta *>(smem + 128);
     uint64_t *slots_s = reinterpret_cast<uint64_t *>(smem + 256);
     float *w_s = reinterpret_cast<float *>(smem + 384);
@@ -243,6 +244,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         C.o_o = (uint32_t)lay.o_o; C.o_h = (uint32_t)lay.o_h; C.o_sel = (uint32_t)lay.o_sel;
         for (int i = 0; i < kStBars; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
+        *iss_s = 0;
     }
     build_pair_table(tab, a.codebook, nullptr);  // ends with __syncthreads
     const int flag0 = ld_ctrl(a.ctrl);
@@ -407,8 +409,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         }
         cta_sync();
         if (*stop_s) break;
-        // the last warp issues the gate/up copies, the one before it the down copies (two
-        // issuing warps halve the issue time)
+        // the last warp issues the gate/up copies; the down rows and the next layer's router
+        // columns wait until the end of C, so that only the copies C needs first are queued
         if (warp == kStProducer) {
             fence_proxy_async_smem();
             const int I = a.I, rowb = C.rowb;
@@ -429,34 +431,12 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     bulk_g2s(gdst + (size_t)n * rowb, base + matb + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
                 }
             }
-            if (threadIdx.x == kColThread && !last) {
-                // then the next layer's router columns, behind the expert copies, and its
-                // residency row into L2 (read once per token, it would come from HBM)
-                if (C.nq > 0) issue_cols(i + 1);
-                if ((E & 1) == 0 && (reinterpret_cast<uintptr_t>(a.table) & 15) == 0)  // 16-byte pieces
-                    prefetch_l2_bulk(a.table + (size_t)(l + 1) * E, (uint32_t)(E * sizeof(uint64_t)));
-            }
-        } else if (warp == kStProducer - 1) {
-            fence_proxy_async_smem();
-            const int K = a.K, I = a.I;
-            const size_t matb = matrix_bytes(I, H);
-            // down: rows [q0, q0 + nq) of every selected expert, completion on bar_dn
-            const int nq = C.nq;
-            if (nq > 0) {
-                const uint32_t bytes = (uint32_t)matrix_bytes(nq, I);
-                if (lane == 0) mbar_arrive_expect_tx(bar_dn, bytes * K);
-                __syncwarp();
-                if (lane < K)
-                    bulk_g2s(smem + C.o_dn + (size_t)lane * C.dtileb,
-                             reinterpret_cast<const uint8_t *>(slots_s[lane]) + 2 * matb + matrix_bytes(C.q0, I), bytes,
-                             bar_dn);
-            }
+            if (lane == 0) *iss_s = 0;
         }
         // the computing warps start once every copy is issued: issued under their load the
         // copies take about three times longer
         cta_sync();
         ex_issued = true;
-        if (!last && C.nq > 0) rc_pend = i + 1;
 
         // ---------------- C: gate/up + SwiGLU of this CTA's pairs ----------------
         if (C.p1 > C.p0) {
@@ -519,7 +499,33 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             }
             if (to) failed = true;
         }
+        // The last warp (whose team has no more rows than any other) then issues the down rows
+        // of the K experts, which D needs after the next grid barrier, the next layer's router
+        // columns and an L2 prefetch of its residency row (read once per token, it would come
+        // from HBM).
+        if (warp == kStProducer && !failed) {
+            fence_proxy_async_smem();
+            const int K = a.K, I = a.I, nq = C.nq;
+            const size_t matb = matrix_bytes(I, H);
+            if (nq > 0) {
+                const uint32_t bytes = (uint32_t)matrix_bytes(nq, I);
+                if (lane == 0) mbar_arrive_expect_tx(bar_dn, bytes * K);
+                __syncwarp();
+                if (lane < K)
+                    bulk_g2s(smem + C.o_dn + (size_t)lane * C.dtileb,
+                             reinterpret_cast<const uint8_t *>(slots_s[lane]) + 2 * matb + matrix_bytes(C.q0, I), bytes,
+                             bar_dn);
+            }
+            if (threadIdx.x == kColThread) {
+                if (!last && nq > 0) issue_cols(i + 1);
+                if (!last && (E & 1) == 0 && (reinterpret_cast<uintptr_t>(a.table) & 15) == 0)  // 16-byte pieces
+                    prefetch_l2_bulk(a.table + (size_t)(l + 1) * E, (uint32_t)(E * sizeof(uint64_t)));
+                *iss_s = (nq > 0 ? 1 : 0) | (!last && nq > 0 ? 2 : 0);
+            }
+            __syncwarp();
+        }
         failed = cta_sync_or(failed) != 0;
+        if (*iss_s & 2) rc_pend = i + 1;
         if (failed) break;
         {
             const int p0 = C.p0, np = C.p1 - C.p0;
@@ -614,6 +620,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         failed = cta_sync_or(failed) != 0;
         if (failed) break;
         ex_issued = false;
+        if (threadIdx.x == 0) *iss_s = 0;  // the down rows have landed (waited above)
         if ((int)threadIdx.x < C.nq) {
             const int r = C.q0 + threadIdx.x;
             const float *o_s = reinterpret_cast<const float *>(smem + C.o_o);
@@ -635,8 +642,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     // ---- exit: no copy into this CTA's shared memory may still be in flight ----
     if (threadIdx.x == 0) {
         if (rc_pend >= 0) mbar_wait(bar_rc, (uint32_t)(rc_pend & 1));
+        if (*iss_s & 1) mbar_wait(bar_dn, ph);
         if (ex_issued) {
-            if (C.nq > 0) mbar_wait(bar_dn, ph);
             for (int bi = 0; bi < 2 * kStGuChunks; ++bi) {
                 const int seg = bi / kStGuChunks, ch = bi % kStGuChunks;
                 if (C.p1 > C.p0 && gu_cut(C, U, seg, ch + 1) > gu_cut(C, U, seg, ch)) mbar_wait(&bar_gu[bi], ph);

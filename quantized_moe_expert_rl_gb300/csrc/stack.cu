@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     int *iss_s = reinterpret_cast<int *>(smem + 76);  // copies issued at the end of C: bit 0 down rows, bit 1 router columns
     StCta &C = *reinterpret_cast<StCta *>(smem + 128);
     uint64_t *slots_s = reinterpret_cast<uint64_t *>(smem + 256);
-    float *w_s = reinterpret_cast<float *>(smem + 384);
+    float *w_s = reinterpret_cast<float *>(smem + 384);   // [K] weights
+    float *sv_s = reinterpret_cast<float *>(smem + 448);  // [K] selected logits (weights computed in D)
     int *pred_s = reinterpret_cast<int *>(smem + 512);  // [kStPredMax] predicted ids of the next layer
     uint4 *tab = reinterpret_cast<uint4 *>(smem + kStHdr);
     constexpr int H = NV * 128;
@@ -377,13 +378,14 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                                           reinterpret_cast<int *>(sb + 8320), my_id, my_val, slot);
             }
             if (warp == 0) {
-                const float w = topk_weight(my_val, K);
                 const int nmiss = __popc(__ballot_sync(kFull, lane < K && slot == 0));
                 const bool bad = __ballot_sync(kFull, lane < K && slot != 0 && (slot & 15)) != 0;
+                const bool stop = nmiss > 0 || bad || flag0 <= l;
                 if (lane < K) {
                     slots_s[lane] = slot;
-                    w_s[lane] = w;
+                    sv_s[lane] = my_val;
                 }
+                __syncwarp();
                 if (blockIdx.x == 0 && a.pg_hits && pregate && i > 0) {
                     // how many of this layer's experts the previous layer predicted
                     bool hit = false;
@@ -394,8 +396,11 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 if (blockIdx.x == 0) {
                     if (lane < K) {
                         a.ids[(size_t)l * K + lane] = my_id;
-                        a.weights[(size_t)l * K + lane] = w;
                         a.slots[(size_t)l * K + lane] = slot;
+                    }
+                    if (stop) {  // the caller resumes from this layer's outputs: its weights now
+                        const float w = topk_weight(my_val, K);
+                        if (lane < K) a.weights[(size_t)l * K + lane] = w;
                     }
                     if (lane == 0 && nmiss > 0) {
                         atomicAdd(a.miss + l, (uint32_t)nmiss);
@@ -403,7 +408,6 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     }
                     if (lane == 0 && bad) dev_error(a.ctrl, RL_DEVERR_SLOT_ALIGN);
                 }
-                const bool stop = nmiss > 0 || bad || flag0 <= l;
                 if (lane == 0) *stop_s = stop;
             }
         }
@@ -538,6 +542,17 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         // acc[i & 1] was read by every CTA in B; it takes the sums of layer index i + 2 next
         if (blockIdx.x == 0)
             for (int j = threadIdx.x; j < E; j += kStThreads) __stcg(a.acc + (size_t)(i & 1) * E + j, 0ll);
+        // the renormalised weights, needed first by the combine (off the path from the
+        // selection to the expert copies); by a warp with the smaller share of the h staging
+        if (warp == kStProducer - 1) {
+            const int K = a.K;
+            const float w = topk_weight(lane < K ? sv_s[lane] : 0.f, K);
+            if (lane < K) {
+                w_s[lane] = w;
+                if (blockIdx.x == 0) a.weights[(size_t)l * K + lane] = w;
+            }
+            __syncwarp();
+        }
         // The producer warp (idle in D when K > 8) meanwhile selects the pre-gated prediction of
         // the next layer's experts and prefetches this CTA's slice of their records into L2
         // ("Red Lite dev23", "What changed": pre-gated expert prefetch).

@@ -25,19 +25,21 @@
 //   B  x_l (L2) -> RMSNorm scale; logits from the accumulators; every CTA selects the top-k
 //      itself (the same code on the same data gives the same ids everywhere, so no further
 //      exchange is needed); CTA 0 writes the outputs, the miss count and the flag; a miss (or
-//      the flag) stops every CTA.  Then the CTA's gate/up rows and down rows of the K selected
-//      experts are copied into shared memory with bulk asynchronous copies, all at once;
-//   C  gate/up + SwiGLU of the CTA's pairs -> h (L2);  grid barrier
-//   D  the CTA's rows of every expert's down projection, the ordered combine and the residual
-//      -> its slice of x_{l+1} (L2), then its router dots of layer l+1 on that slice;
-//      grid barrier.
+//      the flag) stops every CTA.  Then the CTA's gate/up rows of the K selected experts are
+//      copied into shared memory with bulk asynchronous copies;
+//   C  gate/up + SwiGLU of the CTA's pairs -> h (L2); then the last warp copies the CTA's down
+//      rows of the K experts and the next layer's router columns;  grid barrier
+//   D  the renormalised weights (one warp); the CTA's rows of every expert's down projection,
+//      the ordered combine and the residual -> its slice of x_{l+1} (L2), then its router dots
+//      of layer l+1 on that slice;  grid barrier.
+// Only the copies C needs first sit between the selection and the gate/up compute.
 // The arithmetic of every expert row, of the RMSNorm scale and of the selection is the one the
 // per-layer kernels (rl_route, moe_decode) use; the logits differ from rl_route's only by the
 // order of summation (rl_route: one f32 dot per row).
 //
-// Grid barrier: a 64-bit arrival counter in the workspace that only ever grows.  The first
-// arrival of a launch rounds its value down to a multiple of the grid size to find the base,
-// so no reset is needed between launches.  Every spin is bounded: on expiry the CTA sets
+// Grid barrier: a 64-bit arrival counter in the workspace that only ever grows (release
+// reduction to arrive, acquire loads to poll).  The first arrival of a launch rounds its value
+// down to a multiple of the grid size to find the base, so no reset is needed between launches.  Every spin is bounded: on expiry the CTA sets
 // RL_DEVERR_WAIT_TIMEOUT, waits (bounded) for its own copies in flight and returns; the other
 // CTAs then time out at their next barrier.
 #include <cuda.h>

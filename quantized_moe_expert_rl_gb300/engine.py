@@ -15,7 +15,7 @@ resumes the chain at f + 1.  Nothing is evicted: the pool has a slot for every e
 from __future__ import annotations
 
 import time
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 import numpy as np
 import torch
@@ -211,22 +211,39 @@ def enqueue_decode_token_fused(model: Model, b: DecodeBuffers, x_in: torch.Tenso
 @dataclass
 class DecodeStats:
     early_outs: list        # layers at which the chain stopped for a fill
-    filled: list            # (layer, expert) filled
+    filled: list            # (layer, expert) filled at a stop
     fill_bytes: int
-    syncs: int              # host reads of the control block
+    syncs: int              # host reads of the control block or of routing results
+    prefetched: list = field(default_factory=list)  # (layer, expert) filled ahead (lookahead)
 
 
 def run_bounded_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
-                             x_hist: torch.Tensor | None = None, pregate: int = 0) -> DecodeStats:
+                             x_hist: torch.Tensor | None = None, pregate: int = 0,
+                             lookahead: bool = False) -> DecodeStats:
     """One token through every layer with bounded residency ("Red Lite dev23", "What changed",
     item 1): the fused stack runs until a layer f selects an absent expert and stops there
     with y_out = x_f; the host reads the flag once, fills layer f's missing experts, re-resolves
     its slots, runs layer f's experts with the ids and weights the GPU selected, and restarts
-    the stack at f + 1.  The caller zeroes b.miss; b.ctrl is reset here."""
+    the stack at f + 1.  The caller zeroes b.miss; b.ctrl is reset here.
+
+    lookahead: at each stop, before restarting, also route layer f+1 on x_{f+1} (known once
+    layer f has run) and apply layer f+2's router to the same input (the pre-gated prediction
+    of "Red Lite dev23 - per-layer early-out and pre-gated expert prefetch", "What changed":
+    the next layer's router on this layer's input), and fill the absent experts of both, so
+    that the restarted stack stops less often.  Results are unchanged; miss[l] then counts the
+    misses the stack met after those fills."""
     shp, K = model.shape, model.w.top_k
     b.ctrl.copy_(torch.tensor([RL_NO_EARLY_OUT, 0], dtype=torch.int32))
     y_out.copy_(x_in)
     st = DecodeStats([], [], 0, 0)
+    scratch = None
+    if lookahead:
+        d = model.device
+        scratch = dict(ids=torch.zeros((2, K), dtype=torch.int32, device=d),
+                       weights=torch.zeros((2, K), dtype=torch.float32, device=d),
+                       slots=torch.zeros((2, K), dtype=torch.int64, device=d),
+                       miss=torch.zeros(model.L, dtype=torch.int32, device=d),
+                       ctrl=torch.tensor([RL_NO_EARLY_OUT, 0], dtype=torch.int32, device=d))
     l0 = 0
     while l0 < model.L:
         L.moe_decode_stack(shp, l0, model.L - l0, y_out, EPS, model.routers, model.bias, model.table,
@@ -249,6 +266,21 @@ def run_bounded_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor,
         b.ctrl[0] = RL_NO_EARLY_OUT
         L.moe_decode(shp, f, y_out, EPS, b.slots[f], b.weights[f], model.codebook, y_out, 1, b.ctrl, b.dec_ws,
                      b.dec_ws.numel())
+        if scratch is not None and f + 1 < model.L:
+            # layer f+1 on x_{f+1} (exact but for summation order), layer f+2's router on the same
+            # input (the pre-gated prediction); their absent experts are filled now
+            ahead = [f + 1] + ([f + 2] if f + 2 < model.L else [])
+            for j, la in enumerate(ahead):
+                scratch["ctrl"].copy_(torch.tensor([RL_NO_EARLY_OUT, 0], dtype=torch.int32))
+                L.rl_route(shp, la, 1, y_out, EPS, model.routers[la], None if model.bias is None else model.bias[la],
+                           model.table, scratch["ids"][j], scratch["weights"][j], scratch["slots"][j],
+                           scratch["miss"], scratch["ctrl"], None, b.route_ws, b.route_ws.numel())
+            pred = scratch["ids"][:len(ahead)].tolist()
+            st.syncs += 1
+            for la, row in zip(ahead, pred):
+                absent = sorted({e for e in row if not model.resident[la, e]})
+                st.fill_bytes += model.fill(la, absent)
+                st.prefetched += [(la, e) for e in absent]
         l0 = f + 1
     return st
 

@@ -360,3 +360,42 @@ def test_decode_stack_range_flag():
     torch.cuda.synchronize()
     c = b.ctrl.tolist()
     assert c[1] & _lib.RL_DEVERR_RANGE and not (c[1] & _lib.RL_DEVERR_WAIT_TIMEOUT), c
+
+
+def test_decode_stack_bounded_lookahead():
+    """Bounded residency with lookahead fills: at each stop the next layer is routed on its
+    input and the layer after it pre-gated from the same input, and their absent experts are
+    filled before the stack restarts.  The outputs stay bit-identical to a fully resident run;
+    the stack stops no more often than without lookahead, and every expert any layer selected
+    ends up resident."""
+    engine = _engine()
+    base = replace(synth.WORKLOADS["tiny"], n_layers=6)
+    wb = replace(base, n_resident=26)
+    m_full = engine.Model(base)
+    b_full = engine.DecodeBuffers.make(m_full)
+    x = torch.from_numpy(synth.tokens(base, 0, base.tokens)).cuda()
+    stops = {}
+    for look in (False, True):
+        m_b = engine.Model(wb)
+        b_b = engine.DecodeBuffers.make(m_b)
+        n_stop = n_pre = 0
+        for t in range(base.tokens):
+            y_full = torch.zeros(base.hidden, device="cuda")
+            y_b = torch.zeros(base.hidden, device="cuda")
+            engine.enqueue_decode_token_fused(m_full, b_full, x[t], y_full)
+            b_b.miss.zero_()
+            st = engine.run_bounded_decode_token(m_b, b_b, x[t], y_b, lookahead=look)
+            torch.cuda.synchronize()
+            assert torch.equal(_bits(y_full), _bits(y_b)), (look, t)
+            assert torch.equal(_bits(b_full.ids), _bits(b_b.ids)), (look, t)
+            ids = b_full.ids.cpu().numpy()
+            for l in range(wb.n_layers):
+                assert all(m_b.resident[l, int(e)] for e in ids[l]), (look, t, l)
+            n_stop += len(st.early_outs)
+            n_pre += len(st.prefetched)
+            if not look:
+                assert st.prefetched == []
+        stops[look] = (n_stop, n_pre)
+    print(f"bounded decode stops without / with lookahead: {stops[False][0]} / {stops[True][0]}, "
+          f"{stops[True][1]} experts filled ahead")
+    assert stops[True][0] <= stops[False][0] and stops[True][1] > 0

@@ -535,11 +535,27 @@ def bounded_leg(dev, steps: int, warmup: int, path: str = "tc"):
             last = st
     wall = sum(walls) / len(walls)
     fill = sum(fills) / len(fills)
+    # the same chunks with every fill done by the device (rl_fill_missing): one host sync
+    dwalls, dlast = [], None
+    for i in range(warmup + steps):
+        model.reset_residency()
+        x.copy_(x0)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        dst = engine.run_bounded_chunk_device(model, b, x, path=path)
+        torch.cuda.synchronize(dev)
+        if i >= warmup:
+            dwalls.append(time.perf_counter() - t0)
+            dlast = dst
+    dwall = sum(dwalls) / len(dwalls)
     return {"workload": "prefill_bounded (48 layers x 2048 tokens, Zipf 1.1, 435/512 resident)",
             "tokens_per_s_excl_fill": w.tokens / (wall - fill), "tokens_per_s_incl_fill": w.tokens / wall,
             "s_per_chunk": wall, "fill_s_per_chunk": fill, "early_outs": len(last.early_outs),
             "first_early_out": last.first_early_out, "misses_total": sum(last.miss),
-            "experts_filled": len(last.filled), "fill_bytes": last.fill_bytes, "host_syncs": last.syncs}
+            "experts_filled": len(last.filled), "fill_bytes": last.fill_bytes, "host_syncs": last.syncs,
+            "device_fill": {"tokens_per_s": w.tokens / dwall, "s_per_chunk": dwall,
+                            "experts_filled": len(dlast.filled), "misses_total": sum(dlast.miss),
+                            "host_syncs": dlast.syncs}}
 
 
 def main():

@@ -135,6 +135,37 @@ rl_status rl_resolve_slots(const rl_moe_shape *shp, int32_t layer, int32_t T, co
                            const uint64_t *residency, uint64_t *slots, void *stream);
 
 /*
+ * rl_fill_missing - the fill of layer `layer`'s absent selected experts, done by the device
+ * ("Red Lite dev23", "What changed", item 1: the layer's missing experts are loaded and the
+ * layer runs with the experts the router picked), with no host round trip:
+ *   for each distinct expert e with some selection (t, k) of the layer whose slot is 0:
+ *     copy the record (rl_record_bytes) from src[layer][e] to dst[layer][e],
+ *     residency[layer][e] = dst[layer][e], *filled += 1;
+ *   if any: *first_early_out = min(*first_early_out, layer) and, if ctrl[0] == layer,
+ *     ctrl[0] = RL_NO_EARLY_OUT (the layer's experts then run);
+ *   then slots[t][k] = residency[layer][ids[t][k]] for every selection.
+ * Call after rl_route(layer) on the same stream; miss[layer] keeps rl_route's count.
+ * ids int32 [T][K]; slots uint64 [T][K] (in/out); residency uint64 [n_layers][E] (in/out);
+ * src, dst uint64 [n_layers][E]: record addresses the device can read (src: e.g. page-locked
+ * host memory through rl_host_device_pointer) and HBM slots, 16-byte aligned, 0 where there is
+ * none (a needed expert without one sets RL_DEVERR_MISSING, a misaligned one
+ * RL_DEVERR_SLOT_ALIGN; it stays absent); filled uint32 [1] and first_early_out int32 [1]
+ * accumulate.  ws: rl_fill_workspace_bytes(shp) bytes, 16-byte aligned, zero-filled before its
+ * first use (every call leaves it so).
+ */
+size_t rl_fill_workspace_bytes(const rl_moe_shape *shp);
+rl_status rl_fill_missing(const rl_moe_shape *shp, int32_t layer, int32_t T, const int32_t *ids, uint64_t *slots,
+                          uint64_t *residency, const uint64_t *src, const uint64_t *dst, uint32_t *filled,
+                          int32_t *first_early_out, int32_t *ctrl, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * rl_host_device_pointer - (host) the device address of page-locked host memory (host pointer
+ * `host`), for rl_fill_missing's src.  RL_ERR_INVALID when `host` is not page-locked memory
+ * the device can read.
+ */
+rl_status rl_host_device_pointer(const void *host, uint64_t *device);
+
+/*
  * moe_decode - routed experts of ONE token ("Red Lite dev21", "What changed": the
  * single-token expert kernels read the slot table and weights rl_route wrote):
  *   y[h] = (accumulate ? y[h] : 0) + sum_{k=0..K-1, in order} weights[k] * o_k[h],

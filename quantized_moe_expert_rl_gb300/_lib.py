@@ -22,7 +22,7 @@ EXPORTS = ("rl_abi_version", "rl_last_error", "rl_record_bytes", "rl_rmsnorm", "
            "rl_route", "rl_resolve_slots", "moe_decode_workspace_bytes", "moe_decode",
            "rl_build_pairs_workspace_bytes", "rl_build_pairs", "moe_prefill_workspace_bytes",
            "moe_prefill_chunk", "moe_prefill_chunk_f32", "moe_decode_static", "moe_decode_stack_workspace_bytes",
-           "moe_decode_stack")
+           "moe_decode_stack", "rl_fill_workspace_bytes", "rl_fill_missing", "rl_host_device_pointer")
 
 
 class RlShape(ctypes.Structure):
@@ -73,6 +73,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_prefill_workspace_bytes": (sz, [shp, i32]),
         "moe_prefill_chunk": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]),
         "moe_prefill_chunk_f32": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]),
+        "rl_fill_workspace_bytes": (sz, [shp]),
+        "rl_fill_missing": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "rl_host_device_pointer": (i32, [vp, ctypes.POINTER(ctypes.c_uint64)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -127,6 +130,24 @@ def rl_route(shape, layer, T, x, norm_eps, w_router, bias, residency, ids, weigh
     _check("rl_route", load().rl_route(ctypes.byref(shape), layer, T, ptr(x), float(norm_eps), ptr(w_router), ptr(bias),
                                        ptr(residency), ptr(ids), ptr(weights), ptr(slots), ptr(miss), ptr(ctrl),
                                        ptr(logits_out), ptr(ws), ws_bytes, _stream(stream)))
+
+
+def rl_fill_workspace_bytes(shape) -> int:
+    return load().rl_fill_workspace_bytes(ctypes.byref(shape))
+
+
+def rl_fill_missing(shape, layer, T, ids, slots, residency, src, dst, filled, first_early_out, ctrl, ws, ws_bytes,
+                    stream=None):
+    _check("rl_fill_missing", load().rl_fill_missing(ctypes.byref(shape), layer, T, ptr(ids), ptr(slots),
+                                                     ptr(residency), ptr(src), ptr(dst), ptr(filled),
+                                                     ptr(first_early_out), ptr(ctrl), ptr(ws), ws_bytes,
+                                                     _stream(stream)))
+
+
+def rl_host_device_pointer(host_ptr: int) -> int:
+    out = ctypes.c_uint64(0)
+    _check("rl_host_device_pointer", load().rl_host_device_pointer(host_ptr, ctypes.byref(out)))
+    return int(out.value)
 
 
 def rl_resolve_slots(shape, layer, T, ids, residency, slots, stream=None):

@@ -118,6 +118,27 @@ class Model:
             self.table[layer].copy_(row, non_blocking=True)
         return n
 
+    def device_fill_tables(self):
+        """(src, dst) for rl_fill_missing: uint64 [L][E] device tensors holding, for every
+        (layer, expert), the device-readable address of its record in the pinned backing store
+        (0 when it has none) and the address of its HBM slot."""
+        if getattr(self, "_fill_tables", None) is None:
+            E, rb = self.w.n_experts, self.record_bytes
+            src = np.zeros((self.L, E), dtype=np.uint64)
+            if self.backing_index:
+                base = L.rl_host_device_pointer(self.backing.data_ptr())
+                for (l, e), j in self.backing_index.items():
+                    src[l, e] = np.uint64(base + j * rb)
+            self._fill_tables = (torch.from_numpy(src.view(np.int64)).to(self.device),
+                                 torch.from_numpy(self.addr.view(np.int64).copy()).to(self.device))
+        return self._fill_tables
+
+    def sync_residency_from_device(self) -> None:
+        """Bring the host mirror (table_host, resident) up to date after fills done by the
+        device (rl_fill_missing)."""
+        self.table_host = self.table.cpu().numpy().view(np.uint64).copy()
+        self.resident = self.table_host != 0
+
     def reset_residency(self) -> None:
         """Forget fills: mark the seeded absent experts absent again (their slots keep
         whatever bytes they hold; the table no longer points at them)."""
@@ -299,6 +320,8 @@ class PrefillBuffers:
     pair_k: torch.Tensor
     route_ws: torch.Tensor
     ws: torch.Tensor
+    fill_ws: torch.Tensor    # zero-filled: rl_fill_missing's claim flags and list
+    fill_cnt: torch.Tensor   # [filled, first early-out] of device fills
 
     @staticmethod
     def make(model: Model, T: int) -> "PrefillBuffers":
@@ -316,7 +339,9 @@ class PrefillBuffers:
             pair_tok=torch.zeros(max(1, T * K), dtype=torch.int32, device=d),
             pair_k=torch.zeros(max(1, T * K), dtype=torch.uint8, device=d),
             route_ws=torch.zeros(max(256, L.rl_route_workspace_bytes(shp, T)), dtype=torch.uint8, device=d),
-            ws=torch.empty(max(256, L.moe_prefill_workspace_bytes(shp, T)), dtype=torch.uint8, device=d))
+            ws=torch.empty(max(256, L.moe_prefill_workspace_bytes(shp, T)), dtype=torch.uint8, device=d),
+            fill_ws=torch.zeros(max(256, L.rl_fill_workspace_bytes(shp)), dtype=torch.uint8, device=d),
+            fill_cnt=torch.tensor([0, RL_NO_EARLY_OUT], dtype=torch.int32, device=d))
 
 
 def _experts_fn(path: str):
@@ -422,3 +447,43 @@ def run_bounded_chunk(model: Model, b: PrefillBuffers, x: torch.Tensor, path: st
         resume_experts = True
     stats.miss = [int(v) for v in b.miss.cpu().tolist()]
     return stats
+
+
+def run_bounded_chunk_device(model: Model, b: PrefillBuffers, x: torch.Tensor, path: str = "tc",
+                             hist: dict | None = None) -> BoundedStats:
+    """Prefill chunk through model.L stacked layers with bounded residency and every fill done
+    by the device: per layer rl_route (exact miss count, early-out flag), rl_fill_missing (the
+    layer's absent selected experts copied from the pinned backing store into their slots, the
+    slots re-resolved, the flag cleared), then the layer's experts, all enqueued at once with
+    one host sync at the end.  Same selections, fills and outputs as run_bounded_chunk; the
+    early-out layers are the layers that missed.  hist as for run_bounded_chunk."""
+    hist = hist or {}
+    T, shp = x.shape[0], model.shape
+    src, dst = model.device_fill_tables()
+    table0 = model.table_host.copy()
+    b.miss.zero_()
+    b.ctrl[0] = RL_NO_EARLY_OUT
+    b.ctrl[1] = 0
+    b.fill_cnt[0] = 0
+    b.fill_cnt[1] = RL_NO_EARLY_OUT
+    filled, first = b.fill_cnt[0:1], b.fill_cnt[1:2]
+    for l in range(model.L):
+        if "x" in hist:
+            hist["x"][l].copy_(x)
+        enqueue_prefill_route(model, b, l, x, True, keep_logits="logits" in hist)
+        for key, src_t in (("logits", b.logits), ("ids", b.ids), ("weights", b.weights), ("slots", b.slots)):
+            if key in hist:
+                hist[key][l].copy_(src_t)
+        L.rl_fill_missing(shp, l, T, b.ids, b.slots, model.table, src, dst, filled, first, b.ctrl, b.fill_ws,
+                          b.fill_ws.numel())
+        enqueue_prefill_experts(model, b, l, x, x, True, path)
+    ctrl = b.ctrl.cpu()
+    if int(ctrl[1]) != 0:
+        raise RuntimeError(f"device error bits {int(ctrl[1])} in a device-filled chunk")
+    model.sync_residency_from_device()
+    miss = [int(v) for v in b.miss.cpu().tolist()]
+    cnt = b.fill_cnt.cpu().tolist()
+    new = np.argwhere((table0 == 0) & (model.table_host != 0))
+    fl = [(int(l), int(e)) for l, e in new]
+    return BoundedStats(miss, int(cnt[1]), [l for l in range(model.L) if miss[l] > 0], fl,
+                        int(cnt[0]) * model.record_bytes, 0.0, 1)

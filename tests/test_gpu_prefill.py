@@ -136,3 +136,32 @@ def test_prefill_bounded(bounded_model, path, tol):
             worst = max(worst, err)
             assert err <= tol, (l, err)
     print(f"bounded {path}: worst sampled-layer rel L2 {worst:.2e}; near ties {rep.get('near_ties', 0)}")
+
+
+def test_prefill_bounded_device_fill(bounded_model):
+    """The bounded chunk with every fill done by the device (rl_fill_missing, no host round
+    trip) against the host-driven chain on the same seeded residency: identical per-layer miss
+    counts, first early-out layer, filled experts, final residency and outputs (bit for bit)."""
+    engine = _engine()
+    w, m, o = bounded_model
+    T = w.tokens
+    x0 = torch.from_numpy(synth.tokens(w)).cuda()
+    res = {}
+    for mode in ("host", "device"):
+        m.reset_residency()
+        b = engine.PrefillBuffers.make(m, T)
+        x = x0.clone()
+        if mode == "host":
+            st = engine.run_bounded_chunk(m, b, x, path="tc")
+        else:
+            st = engine.run_bounded_chunk_device(m, b, x, path="tc")
+        torch.cuda.synchronize()
+        assert b.ctrl.tolist() == [0x7FFFFFFF, 0], mode
+        res[mode] = (st, x.cpu().view(torch.int32), m.table_host.copy())
+    (sh, xh, th), (sd, xd, td) = res["host"], res["device"]
+    assert sh.miss == sd.miss and sh.first_early_out == sd.first_early_out
+    assert sorted(sh.filled) == sd.filled and sh.fill_bytes == sd.fill_bytes
+    assert np.array_equal(th, td)
+    assert torch.equal(xh, xd)
+    assert sd.syncs == 1 and sum(sd.miss) > 0
+    print(f"device fills: {len(sd.filled)} experts, {sum(sd.miss)} misses, outputs identical to the host path")

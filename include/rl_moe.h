@@ -249,6 +249,25 @@ rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, int32_t n_la
                            uint32_t *pregate_hits, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_decode_stack_fill - moe_decode_stack (no pre-gating) where a layer that selects absent
+ * experts does not stop the launch: the device fills them ("Red Lite dev23", "What changed",
+ * item 1: the layer's missing experts are loaded and it runs with the experts the router
+ * picked).  Every CTA copies its share of each missing record from fill_src[l][e] (an address
+ * the device can read, e.g. page-locked host memory through rl_host_device_pointer) to
+ * fill_dst[l][e] (its HBM slot); after a grid barrier residency[l][e] = slots[l][k] =
+ * fill_dst[l][e], *filled += 1, and the layer runs.  miss[l] still counts the layer's misses;
+ * ctrl[0] is not raised.  A missing expert without a source (0) or with a misaligned address
+ * falls back to moe_decode_stack's stop.  fill_src, fill_dst uint64 [n_layers][E]; filled
+ * uint32 [1] (accumulated).  Same results as the stop / fill / resume flow.
+ */
+rl_status moe_decode_stack_fill(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x, float norm_eps,
+                                const float *w_router, const float *bias, uint64_t *residency,
+                                const int8_t *codebook, int32_t *ids, float *weights, uint64_t *slots,
+                                uint32_t *miss, int32_t *ctrl, float *logits_out, float *x_hist,
+                                const uint64_t *fill_src, const uint64_t *fill_dst, uint32_t *filled, void *ws,
+                                size_t ws_bytes, void *stream);
+
+/*
  * rl_build_pairs - (expert, token) pairs sorted by expert, stable in (t, k) order
  * ("Red Lite dev20", "What changed", item 3):
  *   offs[e] .. offs[e+1]-1 index the pairs of expert e; pair p is (pair_tok[p], pair_k[p]).

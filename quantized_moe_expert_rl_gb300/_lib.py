@@ -22,7 +22,8 @@ EXPORTS = ("rl_abi_version", "rl_last_error", "rl_record_bytes", "rl_rmsnorm", "
            "rl_route", "rl_resolve_slots", "moe_decode_workspace_bytes", "moe_decode",
            "rl_build_pairs_workspace_bytes", "rl_build_pairs", "moe_prefill_workspace_bytes",
            "moe_prefill_chunk", "moe_prefill_chunk_f32", "moe_decode_static", "moe_decode_stack_workspace_bytes",
-           "moe_decode_stack", "rl_fill_workspace_bytes", "rl_fill_missing", "rl_host_device_pointer")
+           "moe_decode_stack", "rl_fill_workspace_bytes", "rl_fill_missing", "rl_host_device_pointer",
+           "moe_decode_stack_fill")
 
 
 class RlShape(ctypes.Structure):
@@ -73,6 +74,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_prefill_workspace_bytes": (sz, [shp, i32]),
         "moe_prefill_chunk": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]),
         "moe_prefill_chunk_f32": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]),
+        "moe_decode_stack_fill": (i32, [shp, i32, i32, vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                        vp, vp, sz, vp]),
         "rl_fill_workspace_bytes": (sz, [shp]),
         "rl_fill_missing": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "rl_host_device_pointer": (i32, [vp, ctypes.POINTER(ctypes.c_uint64)]),
@@ -181,6 +184,14 @@ def moe_decode_stack(shape, layer0, n_layers, x, norm_eps, w_router, bias, resid
         ctypes.byref(shape), layer0, n_layers, ptr(x), float(norm_eps), ptr(w_router), ptr(bias), ptr(residency),
         ptr(codebook), ptr(ids), ptr(weights), ptr(slots), ptr(miss), ptr(ctrl), ptr(logits_out), ptr(x_hist),
         int(pregate), ptr(pregate_hits), ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_decode_stack_fill(shape, layer0, n_layers, x, norm_eps, w_router, bias, residency, codebook, ids, weights,
+                          slots, miss, ctrl, logits_out, x_hist, fill_src, fill_dst, filled, ws, ws_bytes, stream=None):
+    _check("moe_decode_stack_fill", load().moe_decode_stack_fill(
+        ctypes.byref(shape), layer0, n_layers, ptr(x), float(norm_eps), ptr(w_router), ptr(bias), ptr(residency),
+        ptr(codebook), ptr(ids), ptr(weights), ptr(slots), ptr(miss), ptr(ctrl), ptr(logits_out), ptr(x_hist),
+        ptr(fill_src), ptr(fill_dst), ptr(filled), ptr(ws), ws_bytes, _stream(stream)))
 
 
 def rl_build_pairs_workspace_bytes(shape, T) -> int:

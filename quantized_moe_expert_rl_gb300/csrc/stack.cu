@@ -137,6 +137,10 @@ struct StackArgs {
     long long *acc_pg;  // [2][E] the same for the pre-gate dots (next layer's router, this input)
     float *h;           // [K][I]
     uint32_t *pg_hits;  // [L] or NULL
+    uint64_t *table_w;         // the table again, written by device fills (NULL without fill tables)
+    const uint64_t *fill_src;  // [L][E] device-readable record sources, or NULL (stop on a miss instead)
+    const uint64_t *fill_dst;  // [L][E] HBM slots
+    uint32_t *filled;          // experts filled by the device
     int layer0, nl, H, E, K, I, pregate, n_layers;
 };
 
@@ -217,6 +221,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     float *w_s = reinterpret_cast<float *>(smem + 384);   // [K] weights
     float *sv_s = reinterpret_cast<float *>(smem + 448);  // [K] selected logits (weights computed in D)
     int *pred_s = reinterpret_cast<int *>(smem + 512);  // [kStPredMax] predicted ids of the next layer
+    int *fid_s = reinterpret_cast<int *>(smem + 640);    // [K] selected ids, for a device fill
+    uint32_t *fmask_s = reinterpret_cast<uint32_t *>(smem + 704);  // selections k to fill on the device
     uint4 *tab = reinterpret_cast<uint4 *>(smem + kStHdr);
     constexpr int H = NV * 128;
     constexpr int U = H >= 2048 ? 1 : 2048 / H;  // gu_unit(H)
@@ -380,13 +386,25 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                                           reinterpret_cast<int *>(sb + 8320), my_id, my_val, slot);
             }
             if (warp == 0) {
-                const int nmiss = __popc(__ballot_sync(kFull, lane < K && slot == 0));
+                const unsigned mmask = __ballot_sync(kFull, lane < K && slot == 0);
+                const int nmiss = __popc(mmask);
                 const bool bad = __ballot_sync(kFull, lane < K && slot != 0 && (slot & 15)) != 0;
-                const bool stop = nmiss > 0 || bad || flag0 <= l;
+                // with fill tables, a miss whose record has a source is filled here by the device
+                // instead of stopping the launch
+                bool fillable = a.fill_src != nullptr && nmiss > 0;
+                if (fillable) {
+                    const size_t at = (size_t)l * a.E + (lane < K ? my_id : 0);
+                    const bool ok = !(lane < K && slot == 0) ||
+                                    (a.fill_src[at] != 0 && a.fill_dst[at] != 0 && ((a.fill_src[at] | a.fill_dst[at]) & 15) == 0);
+                    fillable = __all_sync(kFull, ok);
+                }
+                const bool stop = (nmiss > 0 && !fillable) || bad || flag0 <= l;
                 if (lane < K) {
                     slots_s[lane] = slot;
                     sv_s[lane] = my_val;
+                    fid_s[lane] = my_id;
                 }
+                if (lane == 0) *fmask_s = fillable && !stop ? mmask : 0u;
                 __syncwarp();
                 if (blockIdx.x == 0 && a.pg_hits && pregate && i > 0) {
                     // how many of this layer's experts the previous layer predicted
@@ -406,7 +424,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     }
                     if (lane == 0 && nmiss > 0) {
                         atomicAdd(a.miss + l, (uint32_t)nmiss);
-                        atomicMin(a.ctrl, l);
+                        if (!fillable) atomicMin(a.ctrl, l);
                     }
                     if (lane == 0 && bad) dev_error(a.ctrl, RL_DEVERR_SLOT_ALIGN);
                 }
@@ -415,10 +433,38 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         }
         cta_sync();
         if (*stop_s) break;
+        if (*fmask_s) {
+            // device fill: every CTA copies its share of each missing record from the fill source
+            // into its slot; after a grid barrier the slots and the table point at them
+            const uint32_t fm = *fmask_s;
+            const size_t rb = 3 * matrix_bytes(a.I, H);
+            const size_t S = align_up((rb + gridDim.x - 1) / gridDim.x, 16);
+            const size_t lo = (size_t)blockIdx.x * S, hi = lo + S < rb ? lo + S : rb;
+            for (int k = 0; k < a.K; ++k) {
+                if (!((fm >> k) & 1u) || lo >= hi) continue;
+                const size_t at = (size_t)l * E + fid_s[k];
+                const uint4 *sp = reinterpret_cast<const uint4 *>(a.fill_src[at] + lo);
+                uint4 *dp = reinterpret_cast<uint4 *>(a.fill_dst[at] + lo);
+                for (size_t j = threadIdx.x; j < (hi - lo) / 16; j += kStThreads) dp[j] = sp[j];
+            }
+            if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
+            if (threadIdx.x < (unsigned)a.K && ((fm >> threadIdx.x) & 1u)) {
+                const size_t at = (size_t)l * E + fid_s[threadIdx.x];
+                const uint64_t d = a.fill_dst[at];
+                slots_s[threadIdx.x] = d;
+                if (blockIdx.x == 0) {
+                    a.table_w[at] = d;
+                    a.slots[(size_t)l * a.K + threadIdx.x] = d;
+                    atomicAdd(a.filled, 1u);
+                }
+            }
+            cta_sync();
+        }
         // the last warp issues the gate/up copies; the down rows and the next layer's router
         // columns wait until the end of C, so that only the copies C needs first are queued
         if (warp == kStProducer) {
             fence_proxy_async_smem();
+            if (a.fill_src) asm volatile("fence.proxy.async.global;" ::: "memory");  // records filled above
             const int I = a.I, rowb = C.rowb;
             const size_t matb = matrix_bytes(I, H);
             // gate/up: lane i < 2 * kStGuChunks issues chunk (segment i / kStGuChunks, part
@@ -511,6 +557,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         // from HBM).
         if (warp == kStProducer && !failed) {
             fence_proxy_async_smem();
+            if (a.fill_src) asm volatile("fence.proxy.async.global;" ::: "memory");
             const int K = a.K, I = a.I, nq = C.nq;
             const size_t matb = matrix_bytes(I, H);
             if (nq > 0) {
@@ -748,12 +795,12 @@ extern "C" size_t moe_decode_stack_workspace_bytes(const rl_moe_shape *shp) {
            align_up((size_t)shp->top_k * shp->inter * sizeof(float), 256);
 }
 
-extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x,
-                                      float norm_eps, const float *w_router, const float *bias,
-                                      const uint64_t *residency, const int8_t *codebook, int32_t *ids,
-                                      float *weights, uint64_t *slots, uint32_t *miss, int32_t *ctrl,
-                                      float *logits_out, float *x_hist, int32_t pregate, uint32_t *pregate_hits,
-                                      void *ws, size_t ws_bytes, void *stream) {
+static rl_status stack_entry(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x, float norm_eps,
+                             const float *w_router, const float *bias, uint64_t *residency, const int8_t *codebook,
+                             int32_t *ids, float *weights, uint64_t *slots, uint32_t *miss, int32_t *ctrl,
+                             float *logits_out, float *x_hist, int32_t pregate, uint32_t *pregate_hits,
+                             const uint64_t *fill_src, const uint64_t *fill_dst, uint32_t *filled, void *ws,
+                             size_t ws_bytes, void *stream) {
     rl_status st = check_shape(shp);
     if (st != RL_OK) return st;
     if (layer0 < 0 || n_layers < 0 || layer0 + n_layers > shp->n_layers)
@@ -792,6 +839,10 @@ extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, i
     a.h = reinterpret_cast<float *>(w8 + 256 + 2 * accb);
     a.pg_hits = pregate_hits;
     a.pregate = pregate;
+    a.table_w = fill_src ? residency : nullptr;
+    a.fill_src = fill_src;
+    a.fill_dst = fill_dst;
+    a.filled = filled;
     a.layer0 = layer0;
     a.nl = n_layers;
     a.n_layers = shp->n_layers;
@@ -806,4 +857,27 @@ extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, i
         case 1024: return launch_stack_i<8, 2, 2>(a, s);
         default: return launch_stack_i<16, 4, 2>(a, s);
     }
+}
+
+extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x,
+                                      float norm_eps, const float *w_router, const float *bias,
+                                      const uint64_t *residency, const int8_t *codebook, int32_t *ids,
+                                      float *weights, uint64_t *slots, uint32_t *miss, int32_t *ctrl,
+                                      float *logits_out, float *x_hist, int32_t pregate, uint32_t *pregate_hits,
+                                      void *ws, size_t ws_bytes, void *stream) {
+    // without fill tables the residency table is only read
+    return stack_entry(shp, layer0, n_layers, x, norm_eps, w_router, bias, const_cast<uint64_t *>(residency),
+                       codebook, ids, weights, slots, miss, ctrl, logits_out, x_hist, pregate, pregate_hits, nullptr,
+                       nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+extern "C" rl_status moe_decode_stack_fill(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x,
+                                           float norm_eps, const float *w_router, const float *bias,
+                                           uint64_t *residency, const int8_t *codebook, int32_t *ids, float *weights,
+                                           uint64_t *slots, uint32_t *miss, int32_t *ctrl, float *logits_out,
+                                           float *x_hist, const uint64_t *fill_src, const uint64_t *fill_dst,
+                                           uint32_t *filled, void *ws, size_t ws_bytes, void *stream) {
+    if (!fill_src || !fill_dst || !filled) return fail(RL_ERR_INVALID, "moe_decode_stack_fill: NULL fill argument");
+    return stack_entry(shp, layer0, n_layers, x, norm_eps, w_router, bias, residency, codebook, ids, weights, slots,
+                       miss, ctrl, logits_out, x_hist, 0, nullptr, fill_src, fill_dst, filled, ws, ws_bytes, stream);
 }

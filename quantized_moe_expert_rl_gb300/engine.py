@@ -306,6 +306,22 @@ def run_bounded_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor,
     return st
 
 
+def run_bounded_decode_token_device(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
+                                    filled: torch.Tensor, x_hist: torch.Tensor | None = None) -> None:
+    """One token through every layer with bounded residency in ONE launch: a layer that selects
+    absent experts has them copied by the device from the pinned backing store into their slots
+    and runs on (moe_decode_stack_fill); b.miss counts the misses per layer, `filled` (uint32
+    [1], accumulated) the experts filled.  Same results as run_bounded_decode_token.  The caller
+    zeroes b.miss; b.ctrl is reset here; call model.sync_residency_from_device() before using
+    the host mirror of the table."""
+    src, dst = model.device_fill_tables()
+    b.ctrl.copy_(torch.tensor([RL_NO_EARLY_OUT, 0], dtype=torch.int32))
+    y_out.copy_(x_in)
+    L.moe_decode_stack_fill(model.shape, 0, model.L, y_out, EPS, model.routers, model.bias, model.table,
+                            model.codebook, b.ids, b.weights, b.slots, b.miss, b.ctrl, None, x_hist, src, dst, filled,
+                            b.stack_ws, b.stack_ws.numel())
+
+
 @dataclass
 class PrefillBuffers:
     xn: torch.Tensor

@@ -399,3 +399,39 @@ def test_decode_stack_bounded_lookahead():
     print(f"bounded decode stops without / with lookahead: {stops[False][0]} / {stops[True][0]}, "
           f"{stops[True][1]} experts filled ahead")
     assert stops[True][0] <= stops[False][0] and stops[True][1] > 0
+
+
+def test_decode_stack_device_fill():
+    """Bounded residency with the fills done inside the fused launch (moe_decode_stack_fill):
+    no stop, the same per-layer miss counts and fills as the stop / fill / resume flow, outputs
+    bit-identical to a fully resident model."""
+    engine = _engine()
+    base = replace(synth.WORKLOADS["tiny"], n_layers=6)
+    wb = replace(base, n_resident=26)
+    m_full, m_h, m_d = engine.Model(base), engine.Model(wb), engine.Model(wb)
+    b_full, b_h, b_d = (engine.DecodeBuffers.make(m) for m in (m_full, m_h, m_d))
+    x = torch.from_numpy(synth.tokens(base, 0, base.tokens)).cuda()
+    filled = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n_host_fills = 0
+    for t in range(base.tokens):
+        y_full, y_h, y_d = (torch.zeros(base.hidden, device="cuda") for _ in range(3))
+        engine.enqueue_decode_token_fused(m_full, b_full, x[t], y_full)
+        b_h.miss.zero_()
+        st = engine.run_bounded_decode_token(m_h, b_h, x[t], y_h)
+        b_d.miss.zero_()
+        engine.run_bounded_decode_token_device(m_d, b_d, x[t], y_d, filled)
+        torch.cuda.synchronize()
+        assert b_d.ctrl.tolist() == [0x7FFFFFFF, 0], t
+        assert torch.equal(_bits(y_full), _bits(y_d)), t
+        assert torch.equal(_bits(y_h), _bits(y_d)), t
+        assert b_h.miss.tolist() == b_d.miss.tolist(), t
+        assert torch.equal(_bits(b_h.ids), _bits(b_d.ids)), t
+        # the two models have their own pools: compare slots as offsets into them
+        oh = b_h.slots.cpu() - m_h.pool.data_ptr()
+        od = b_d.slots.cpu() - m_d.pool.data_ptr()
+        assert torch.equal(oh, od), t
+        n_host_fills += len(st.filled)
+    m_d.sync_residency_from_device()
+    assert np.array_equal(m_d.resident, m_h.resident)
+    assert int(filled.item()) == n_host_fills > 0
+    print(f"device fills inside the fused launch: {n_host_fills} experts over {base.tokens} tokens, no stop")

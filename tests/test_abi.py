@@ -102,3 +102,32 @@ def test_decode_stack_host_checks(lib):
     assert lib.moe_decode_stack(ctypes.byref(s), 0, 48, *bad, need, None) == RL_ERR_INVALID
     # zero layers: nothing to do, no launch
     assert lib.moe_decode_stack(ctypes.byref(s), 48, 0, *args, need, None) == RL_OK
+
+
+def test_fill_host_checks(lib):
+    """rl_fill_missing, moe_decode_stack_fill and rl_host_device_pointer: the checks made
+    before any launch (no GPU needed)."""
+    from quantized_moe_expert_rl_gb300._lib import RL_ERR_INVALID, RlShape
+    s = RlShape.of(2048, 512, 10, 512, 48)
+    need = lib.rl_fill_workspace_bytes(ctypes.byref(s))
+    assert need >= 512 * 8
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake] * 8   # ids, slots, residency, src, dst, filled, first_early_out, ctrl
+    assert lib.rl_fill_missing(ctypes.byref(s), 48, 4, *args, fake, need, None) == RL_ERR_INVALID
+    assert b"layer" in lib.rl_last_error()
+    assert lib.rl_fill_missing(ctypes.byref(s), 0, 4, *args, fake, need - 8, None) == RL_ERR_INVALID
+    assert b"workspace" in lib.rl_last_error()
+    bad = list(args)
+    bad[3] = None
+    assert lib.rl_fill_missing(ctypes.byref(s), 0, 4, *bad, fake, need, None) == RL_ERR_INVALID
+    # the fused decode with fills needs its fill tables
+    need_st = lib.moe_decode_stack_workspace_bytes(ctypes.byref(s))
+    st_args = [fake, -1.0, fake, None, fake, fake, fake, fake, fake, fake, fake, None, None]
+    assert lib.moe_decode_stack_fill(ctypes.byref(s), 0, 48, *st_args, None, fake, fake, fake, need_st,
+                                     None) == RL_ERR_INVALID
+    assert b"fill" in lib.rl_last_error()
+    # a pointer that is not page-locked host memory has no device address
+    out = ctypes.c_uint64(0)
+    buf = ctypes.create_string_buffer(64)
+    assert lib.rl_host_device_pointer(ctypes.cast(buf, ctypes.c_void_p), ctypes.byref(out)) == RL_ERR_INVALID
+    assert lib.rl_host_device_pointer(None, ctypes.byref(out)) == RL_ERR_INVALID

@@ -55,29 +55,42 @@ def _tensor_peak():
         return 1900.0, "fallback bf16_tflops"
 
 
-def _src_digest() -> str:
-    """Digest of the kernel sources' code: comments and blank space are left out, so that a
-    change of comments alone keeps the recorded DRAM traffic valid."""
+# The translation unit that holds each profiled kernel: its recorded DRAM traffic stays valid
+# while the code of that file and of every header it includes is unchanged.
+_KERNEL_TU = {"moe_decode_stack": "stack.cu", "moe_decode": "decode.cu", "tc_gemm": "prefill_tc.cu"}
+
+
+def _src_digest(kernel: str, root: str = ROOT) -> str:
+    """Digest of the code of `kernel`'s translation unit (the .cu file and, transitively, the
+    quoted includes found in csrc/ or include/): comments and blank space are left out, so that
+    a change of comments alone keeps the recorded DRAM traffic valid."""
     import re
-    h = hashlib.sha256()
-    cdir = os.path.join(ROOT, "quantized_moe_expert_rl_gb300", "csrc")
-    for f in sorted(os.listdir(cdir)):
-        if f.endswith((".cu", ".cuh")):
-            src = open(os.path.join(cdir, f), encoding="utf-8").read()
-            src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
-            src = re.sub(r"//[^\n]*", " ", src)
-            h.update(" ".join(src.split()).encode())
+    dirs = [os.path.join(root, "quantized_moe_expert_rl_gb300", "csrc"), os.path.join(root, "include")]
+    h, seen, todo = hashlib.sha256(), set(), [_KERNEL_TU[kernel]]
+    while todo:
+        name = todo.pop(0)
+        if name in seen:
+            continue
+        seen.add(name)
+        path = next((os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name))), None)
+        if path is None:
+            raise FileNotFoundError(name)
+        src = open(path, encoding="utf-8").read()
+        todo += re.findall(r'^\s*#\s*include\s+"([^"]+)"', src, flags=re.M)
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(name.encode() + b"\0" + " ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
 def _traffic(kernel: str, units: float):
     """DRAM bytes per launch of `kernel` from the committed ncu capture summary, scaled to
-    the launch's work; None when absent or when the kernel sources changed since."""
+    the launch's work; None when absent or when the kernel's translation unit changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))
         e = d[kernel]
-        if e.get("src_digest") != _src_digest():
+        if e.get("src_digest") != _src_digest(kernel):
             return None
         return float(e["dram_bytes_per_unit"]) * units
     except Exception:
@@ -233,11 +246,12 @@ def run_reference(a):
             per_step.append(rate)
     value = sum(per_step) / len(per_step)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": a.gpus,
-            "steps": a.steps, "warmup": a.warmup, "ms_per_step": None, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000.0 * w.tokens / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config(w, a),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"per step: {sample}"},
+                             "sample": f"per step: {sample}; ms_per_step is the time a whole step of "
+                                       f"{w.tokens} tokens takes at that rate"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

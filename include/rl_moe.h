@@ -44,6 +44,11 @@
  *     sign mask ? -1 : +1).  An expert record is [gate I x H | up I x H |
  *     down H x I] back to back (rl_record_bytes), at a 16-byte aligned slot
  *     address.  Expert output o = down(silu(gate x) * (up x)).
+ *   - Empty input: rl_rmsnorm, rl_route, rl_resolve_slots, rl_build_pairs and
+ *     moe_prefill_chunk(_f32) accept T = 0.  Once the shape and the layer are
+ *     valid they return RL_OK without reading their per-token buffers, which
+ *     may then be NULL; offs and ctrl are still required where a call takes
+ *     them, and rl_build_pairs still writes offs = 0.
  *   - Supported shapes: hidden in {256, 512, 1024, 2048}; inter in {128, 256,
  *     512, 1024, 2048}; 1 <= top_k <= 16; top_k <= n_experts <= 512;
  *     top_k * inter <= 16384; n_layers >= 1.

@@ -90,11 +90,17 @@ def load(path: str | None = None) -> ctypes.CDLL:
 
 
 def ptr(t) -> int | None:
-    """Raw address of a tensor / int / None (NULL)."""
+    """Raw address of a device tensor / int / None (NULL).  The library reads every buffer as
+    a dense array on the device, so a strided view or a host tensor is refused here rather
+    than read wrongly."""
     if t is None:
         return None
     if isinstance(t, int):
         return t or None
+    if not t.is_contiguous():
+        raise ValueError(f"tensor of shape {tuple(t.shape)} and strides {t.stride()} is not contiguous")
+    if t.device.type != "cuda":
+        raise ValueError(f"tensor on {t.device} passed where a device buffer is expected")
     return t.data_ptr() or None
 
 

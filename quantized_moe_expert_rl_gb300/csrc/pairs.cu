@@ -104,7 +104,9 @@ extern "C" rl_status rl_build_pairs(const rl_moe_shape *shp, int32_t layer, int3
     rl_status st = check_shape(shp);
     if (st != RL_OK) return st;
     if (layer < 0 || layer >= shp->n_layers) return fail(RL_ERR_INVALID, "rl_build_pairs: layer %d", layer);
-    if (T < 0 || !ids || !offs || !ctrl || (T > 0 && (!pair_tok || !pair_k)))
+    // offs and ctrl are always needed (T = 0 still writes offs = 0); the per-selection
+    // buffers only when there are selections
+    if (T < 0 || !offs || !ctrl || (T > 0 && (!ids || !pair_tok || !pair_k)))
         return fail(RL_ERR_INVALID, "rl_build_pairs: bad arguments");
     const long long P = (long long)T * shp->top_k;
     if (P > (1ll << 30)) return fail(RL_ERR_UNSUPPORTED, "rl_build_pairs: %lld pairs", P);

@@ -289,12 +289,12 @@ static rl_status launch_route1_n(bool norm, const float *x, float eps, const flo
 using namespace rl;
 
 extern "C" rl_status rl_rmsnorm(const float *x, float *xn, int32_t T, int32_t H, float eps, void *stream) {
-    if (!x || !xn) return fail(RL_ERR_INVALID, "rl_rmsnorm: NULL buffer");
     if (T < 0 || H <= 0 || (H % 128)) return fail(RL_ERR_INVALID, "rl_rmsnorm: bad T=%d or H=%d", T, H);
     if (!(eps >= 0.f)) return fail(RL_ERR_INVALID, "rl_rmsnorm: eps must be >= 0");
+    if (T == 0) return RL_OK;  // no rows: the buffers are not read (they may be NULL)
+    if (!x || !xn) return fail(RL_ERR_INVALID, "rl_rmsnorm: NULL buffer");
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xn)) & 15)
         return fail(RL_ERR_INVALID, "rl_rmsnorm: buffers must be 16-byte aligned");
-    if (T == 0) return RL_OK;
     rmsnorm_kernel<<<T, 256, 0, as_stream(stream)>>>(x, xn, H, eps);
     return check_launch("rl_rmsnorm");
 }
@@ -313,6 +313,7 @@ extern "C" rl_status rl_route(const rl_moe_shape *shp, int32_t layer, int32_t T,
     if (layer < 0 || layer >= shp->n_layers)
         return fail(RL_ERR_INVALID, "rl_route: layer %d outside [0,%d)", layer, shp->n_layers);
     if (T < 0) return fail(RL_ERR_INVALID, "rl_route: T=%d", T);
+    if (T == 0) return RL_OK;  // no tokens: nothing is read or written (buffers may be NULL)
     if (!x || !w_router || !residency || !ids || !weights || !slots || !miss || !ctrl)
         return fail(RL_ERR_INVALID, "rl_route: NULL required buffer");
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router) |
@@ -323,7 +324,6 @@ extern "C" rl_status rl_route(const rl_moe_shape *shp, int32_t layer, int32_t T,
     const RouteWs L(T, E, H, norm);
     if (!ws || ws_bytes < L.total)
         return fail(RL_ERR_INVALID, "rl_route: workspace of %zu B needed, %zu given", L.total, ws_bytes);
-    if (T == 0) return RL_OK;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     unsigned *counter = reinterpret_cast<unsigned *>(w8);
     float *logits = logits_out ? logits_out : reinterpret_cast<float *>(w8 + L.logits);
@@ -373,9 +373,10 @@ extern "C" rl_status rl_resolve_slots(const rl_moe_shape *shp, int32_t layer, in
     rl_status st = check_shape(shp);
     if (st != RL_OK) return st;
     if (layer < 0 || layer >= shp->n_layers) return fail(RL_ERR_INVALID, "rl_resolve_slots: layer %d", layer);
-    if (T < 0 || !ids || !residency || !slots) return fail(RL_ERR_INVALID, "rl_resolve_slots: bad arguments");
+    if (T < 0) return fail(RL_ERR_INVALID, "rl_resolve_slots: T=%d", T);
+    if (T == 0) return RL_OK;  // no tokens: the buffers are not read (they may be NULL)
+    if (!ids || !residency || !slots) return fail(RL_ERR_INVALID, "rl_resolve_slots: NULL buffer");
     const int n = T * shp->top_k;
-    if (n == 0) return RL_OK;
     resolve_slots_kernel<<<(n + 255) / 256, 256, 0, as_stream(stream)>>>(
         ids, residency + (size_t)layer * shp->n_experts, slots, n, shp->n_experts);
     return check_launch("rl_resolve_slots");

@@ -131,3 +131,34 @@ def test_fill_host_checks(lib):
     buf = ctypes.create_string_buffer(64)
     assert lib.rl_host_device_pointer(ctypes.cast(buf, ctypes.c_void_p), ctypes.byref(out)) == RL_ERR_INVALID
     assert lib.rl_host_device_pointer(None, ctypes.byref(out)) == RL_ERR_INVALID
+
+
+def test_binding_refuses_strided_and_host_tensors():
+    """The binding passes raw addresses; a view with gaps or a host tensor would be read as
+    something else by the kernels, so it is refused before any call."""
+    torch = pytest.importorskip("torch")
+    from quantized_moe_expert_rl_gb300._lib import ptr
+    assert ptr(None) is None and ptr(0) is None and ptr(4096) == 4096
+    with pytest.raises(ValueError, match="contiguous"):
+        ptr(torch.zeros(4, 4)[:, 1])
+    with pytest.raises(ValueError, match="device buffer"):
+        ptr(torch.zeros(4))
+
+
+def test_zero_tokens_is_a_no_op(lib):
+    """T = 0: rl_route, rl_rmsnorm, rl_resolve_slots and the prefill chunk return RL_OK
+    without a launch and without reading their per-token buffers (NULL here); a bad layer or
+    a negative T is still refused."""
+    from quantized_moe_expert_rl_gb300._lib import RL_ERR_INVALID, RL_OK, RlShape
+    s = RlShape.of(2048, 512, 10, 512, 48)
+    fake = ctypes.c_void_p(1 << 20)
+    n = [None] * 9
+    assert lib.rl_route(ctypes.byref(s), 3, 0, None, -1.0, *n, None, 0, None) == RL_OK
+    assert lib.rl_route(ctypes.byref(s), 48, 0, None, -1.0, *n, None, 0, None) == RL_ERR_INVALID
+    assert lib.rl_route(ctypes.byref(s), 3, -1, None, -1.0, *n, None, 0, None) == RL_ERR_INVALID
+    assert lib.rl_rmsnorm(None, None, 0, 2048, 1e-6, None) == RL_OK
+    assert lib.rl_rmsnorm(None, None, 1, 2048, 1e-6, None) == RL_ERR_INVALID
+    assert lib.rl_resolve_slots(ctypes.byref(s), 3, 0, None, None, None, None) == RL_OK
+    for fn in (lib.moe_prefill_chunk, lib.moe_prefill_chunk_f32):
+        assert fn(ctypes.byref(s), 3, 0, None, fake, None, None, None, None, None, None, 0, fake, None, 0,
+                  None) == RL_OK

@@ -34,7 +34,7 @@ Sources (the Red Lite engine notes):
           selection order; stacks use x <- x + MoE(RMSNorm(x)), unit gain,
           eps 1e-6; bounded residency adds a Zipf router bias.
 
-Readings where the sources are silent (each is listed in the design doc):
+Readings where the sources are silent (the numbering is shared with the library's docs):
   R1 block bytes: d little-endian at bytes 0-1; group g at bytes 2+2g (idx)
      and 3+2g (sign); bit j of the sign byte (LSB = bit 0) negates value j.
   R2 a matrix is stored flat and row-major in consecutive 256-value blocks

@@ -3,7 +3,8 @@
 #include <stdio.h>
 
 #include <mutex>
-#include <unordered_map>
+#include <map>
+#include <utility>
 
 #include "rl_common.cuh"
 
@@ -41,15 +42,21 @@ rl_status check_shape(const rl_moe_shape *shp) {
     return RL_OK;
 }
 
+// The attribute belongs to the kernel on the current device, so the cache is per device: a
+// process that drives several GPUs sets it once on each.
 rl_status allow_smem(const void *kernel, size_t bytes) {
     static std::mutex mu;
-    static std::unordered_map<const void *, size_t> done;
+    static std::map<std::pair<int, const void *>, size_t> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(RL_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     std::lock_guard<std::mutex> lk(mu);
-    auto it = done.find(kernel);
+    const auto key = std::make_pair(dev, kernel);
+    auto it = done.find(key);
     if (it != done.end() && it->second >= bytes) return RL_OK;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return fail(RL_ERR_CUDA, "cudaFuncSetAttribute(%zu B smem): %s", bytes, cudaGetErrorString(e));
-    done[kernel] = bytes;
+    done[key] = bytes;
     return RL_OK;
 }
 

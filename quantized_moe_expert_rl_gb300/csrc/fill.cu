@@ -133,6 +133,7 @@ extern "C" rl_status rl_fill_missing(const rl_moe_shape *shp, int32_t layer, int
     const size_t rb = 3 * matrix_bytes(shp->inter, shp->hidden);
     if (rb % 16 != 0 || rb > 0xffffffffull)
         return fail(RL_ERR_UNSUPPORTED, "rl_fill_missing: record of %zu B is not a 16-byte multiple", rb);
+    if ((long long)T * shp->top_k > (1ll << 30)) return fail(RL_ERR_UNSUPPORTED, "rl_fill_missing: too many selections");
     const int n = T * shp->top_k;
     if (n == 0) return RL_OK;
     cudaStream_t s = as_stream(stream);

@@ -314,6 +314,7 @@ extern "C" rl_status rl_route(const rl_moe_shape *shp, int32_t layer, int32_t T,
         return fail(RL_ERR_INVALID, "rl_route: layer %d outside [0,%d)", layer, shp->n_layers);
     if (T < 0) return fail(RL_ERR_INVALID, "rl_route: T=%d", T);
     if (T == 0) return RL_OK;  // no tokens: nothing is read or written (buffers may be NULL)
+    if ((long long)T * shp->top_k > (1ll << 30)) return fail(RL_ERR_UNSUPPORTED, "rl_route: too many selections");
     if (!x || !w_router || !residency || !ids || !weights || !slots || !miss || !ctrl)
         return fail(RL_ERR_INVALID, "rl_route: NULL required buffer");
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router) |
@@ -376,6 +377,7 @@ extern "C" rl_status rl_resolve_slots(const rl_moe_shape *shp, int32_t layer, in
     if (T < 0) return fail(RL_ERR_INVALID, "rl_resolve_slots: T=%d", T);
     if (T == 0) return RL_OK;  // no tokens: the buffers are not read (they may be NULL)
     if (!ids || !residency || !slots) return fail(RL_ERR_INVALID, "rl_resolve_slots: NULL buffer");
+    if ((long long)T * shp->top_k > (1ll << 30)) return fail(RL_ERR_UNSUPPORTED, "rl_resolve_slots: too many selections");
     const int n = T * shp->top_k;
     resolve_slots_kernel<<<(n + 255) / 256, 256, 0, as_stream(stream)>>>(
         ids, residency + (size_t)layer * shp->n_experts, slots, n, shp->n_experts);

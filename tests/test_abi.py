@@ -162,3 +162,21 @@ def test_zero_tokens_is_a_no_op(lib):
     for fn in (lib.moe_prefill_chunk, lib.moe_prefill_chunk_f32):
         assert fn(ctypes.byref(s), 3, 0, None, fake, None, None, None, None, None, None, 0, fake, None, 0,
                   None) == RL_OK
+
+
+def test_selection_counts_beyond_the_index_range_are_refused(lib):
+    """T * top_k above 2^30 selections would overflow the kernels' 32-bit pair indices: every
+    entry point that takes T refuses it on the host."""
+    from quantized_moe_expert_rl_gb300._lib import RL_ERR_UNSUPPORTED, RlShape
+    s = RlShape.of(2048, 512, 16, 512, 48)
+    T = (1 << 26) + 1                          # 16 * T > 2^30
+    fake = ctypes.c_void_p(1 << 20)
+    ws = lib.rl_route_workspace_bytes(ctypes.byref(s), T)
+    assert lib.rl_route(ctypes.byref(s), 0, T, fake, -1.0, fake, None, fake, fake, fake, fake, fake, fake, None,
+                        fake, ws, None) == RL_ERR_UNSUPPORTED
+    assert lib.rl_resolve_slots(ctypes.byref(s), 0, T, fake, fake, fake, None) == RL_ERR_UNSUPPORTED
+    assert lib.rl_build_pairs(ctypes.byref(s), 0, T, fake, fake, fake, fake, fake, None, 0, None) == RL_ERR_UNSUPPORTED
+    need = lib.rl_fill_workspace_bytes(ctypes.byref(s))
+    assert lib.rl_fill_missing(ctypes.byref(s), 0, T, *([fake] * 8), fake, need, None) == RL_ERR_UNSUPPORTED
+    for fn in (lib.moe_prefill_chunk, lib.moe_prefill_chunk_f32):
+        assert fn(ctypes.byref(s), 0, T, *([fake] * 7), fake, 0, fake, fake, 1 << 62, None) == RL_ERR_UNSUPPORTED

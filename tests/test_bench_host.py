@@ -53,3 +53,40 @@ def test_recorded_traffic_is_per_launch():
     # the decode stack moves its algorithmic bytes and little more (no re-reads)
     alg = 48 * (10 * 811008 + 512 * 2048 * 4 + 2 * 2048 * 4)
     assert 1.0 <= d["moe_decode_stack"]["dram_bytes_per_unit"] / alg < 1.01
+
+
+def test_clock_summary_reads_reasons_and_median():
+    """nvidia-smi lines (index, clocks.sm, clocks.max.sm, power, active mask, hw_slowdown,
+    hw_thermal, sw_thermal, sw_power_cap) -> median SM clock, max clock, active reasons."""
+    c = bench.ClockSampler(0)
+    c.lines = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 1900, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+               "0, 2055, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "garbage line", ""]
+    s = c.summary()
+    assert s == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    c.lines = ["0, 1200, 2070, 700.0, 0x8, Active, Not Active, Active, Not Active"]
+    assert c.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    c.lines = []
+    assert c.summary()["reasons"] == ["unsampled"]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """--impl reference on CPU: one JSON line with the keys of the bench contract, the oracle
+    timed on this host's cores over a bounded sample."""
+    import subprocess
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3", "--ref-step-s", "0.5"], capture_output=True, text=True, timeout=600,
+                       env=dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0"))
+    assert p.returncode == 0, p.stderr
+    lines = [ln for ln in p.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 3 and d["value"] > 0
+    assert d["config"]["workload"] == "decode_stack" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert abs(d["ms_per_step"] - 1000.0 * d["config"]["tokens_per_step"] / d["value"]) < 1e-6 * d["ms_per_step"]

@@ -80,6 +80,9 @@ typedef enum rl_status {
 #define RL_DEVERR_BAD_ID 4       /* an expert id outside [0, n_experts) was read */
 #define RL_DEVERR_MISSING 8      /* an expert kernel met a zero (absent) slot */
 #define RL_DEVERR_RANGE 16       /* moe_decode_stack: a router partial sum outside the fixed-point range */
+#define RL_DEVERR_NAN 32         /* a router logit was NaN; NaN ranks below every number (never
+                                    selected while K numbers remain), so inputs holding NaN
+                                    are refused through this bit */
 
 /* (host) model shape, passed by pointer to every call */
 typedef struct rl_moe_shape {

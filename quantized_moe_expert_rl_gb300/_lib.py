@@ -15,6 +15,7 @@ from .build import LIB
 RL_OK, RL_ERR_INVALID, RL_ERR_UNSUPPORTED, RL_ERR_CUDA, RL_ERR_TIMEOUT = 0, 1, 2, 3, 4
 RL_NO_EARLY_OUT = 0x7FFFFFFF
 RL_DEVERR_SLOT_ALIGN, RL_DEVERR_WAIT_TIMEOUT, RL_DEVERR_BAD_ID, RL_DEVERR_MISSING, RL_DEVERR_RANGE = 1, 2, 4, 8, 16
+RL_DEVERR_NAN = 32
 STATUS_NAMES = {0: "RL_OK", 1: "RL_ERR_INVALID", 2: "RL_ERR_UNSUPPORTED", 3: "RL_ERR_CUDA", 4: "RL_ERR_TIMEOUT"}
 
 # every symbol include/rl_moe.h declares

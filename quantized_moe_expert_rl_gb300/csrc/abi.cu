@@ -38,7 +38,7 @@ rl_status check_shape(const rl_moe_shape *shp) {
     if (K > 16) return fail(RL_ERR_UNSUPPORTED, "top_k=%d > 16", K);
     if (E > 512) return fail(RL_ERR_UNSUPPORTED, "n_experts=%d > 512", E);
     if (K > E) return fail(RL_ERR_INVALID, "top_k=%d > n_experts=%d", K, E);
-    if ((size_t)K * I > 16384) return fail(RL_ERR_UNSUPPORTED, "top_k*inter=%d > 16384", K * I);
+    if ((size_t)K * I > (size_t)kMaxKxI) return fail(RL_ERR_UNSUPPORTED, "top_k*inter=%d > %d", K * I, kMaxKxI);
     return RL_OK;
 }
 

@@ -346,6 +346,9 @@ extern "C" rl_status moe_decode(const rl_moe_shape *shp, int32_t layer, const fl
 // call overwrites every h entry it later reads, so nothing needs clearing between calls.
 // ---------------------------------------------------------------------------------------------
 static __device__ __align__(256) float g_static_h[RL_STATIC_SCRATCH_FLOATS];
+// every shape check_shape accepts fits the array, so the size check below only guards a
+// future widening of the supported shapes
+static_assert(RL_STATIC_SCRATCH_FLOATS >= rl::kMaxKxI, "the fixed h scratch must hold top_k * inter floats");
 
 namespace rl {
 // Device address of g_static_h on the current device.  In host code the array's name is

@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1) tc_gemm_kernel(PrefillArgs a, 
     __syncthreads();
     if (tid == kTcMmaWarp * 32) {
         tc::commit(fin_bar);
-        mbar_wait(fin_bar, 0);
+        if (!mbar_wait(fin_bar, 0)) dev_error(a.ctrl, RL_DEVERR_WAIT_TIMEOUT);  // the drain did not finish
     }
     tc::fence_before();
     __syncthreads();

@@ -14,6 +14,8 @@ constexpr int kBlockValues = 256;
 constexpr int kBlockBytes = 66;
 constexpr int kGridBytes = 256 * 8;
 constexpr unsigned kFull = 0xffffffffu;
+// largest top_k * inter of a supported shape (check_shape refuses more)
+constexpr int kMaxKxI = 16384;
 // Bounded on-chip waits: try_wait suspends for a hardware-defined slice, so this cap is
 // far beyond any legitimate wait (seconds) yet finite.
 constexpr uint32_t kWaitCap = 1u << 24;

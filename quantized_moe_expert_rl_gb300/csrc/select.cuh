@@ -16,8 +16,11 @@ namespace rl {
 
 constexpr int kMaxK = 16;  // largest top-k the library accepts
 
+// A NaN logit gets key 0: it ranks below every number, like an absent candidate (the callers
+// raise RL_DEVERR_NAN for it).
 __device__ __forceinline__ uint32_t order_key(float v) {
     const uint32_t b = __float_as_uint(v + 0.0f);  // -0.0 + 0.0 = +0.0
+    if (v != v) return 0u;
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 __device__ __forceinline__ float key_value(uint32_t k) {
@@ -59,10 +62,20 @@ __device__ __forceinline__ void warp_topk_by(KeyOf key_of, int K, int &my_id, fl
     }
 }
 
-// warp_topk_by on E logits read through L2 (they may come from other CTAs)
+// warp_topk_by on E logits read through L2 (they may come from other CTAs); true in every lane
+// when one of the logits was NaN
 template <int C>
-__device__ __forceinline__ void warp_topk(const float *lg, int E, int K, int &my_id, float &my_val) {
-    warp_topk_by<C>([&](int e) { return e < E ? order_key(__ldcg(lg + e)) : 0u; }, K, my_id, my_val);
+__device__ __forceinline__ bool warp_topk(const float *lg, int E, int K, int &my_id, float &my_val) {
+    bool nan = false;
+    warp_topk_by<C>(
+        [&](int e) {
+            if (e >= E) return 0u;
+            const float v = __ldcg(lg + e);
+            nan |= v != v;
+            return order_key(v);
+        },
+        K, my_id, my_val);
+    return __any_sync(kFull, nan);
 }
 
 // w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0), the sum taken in selection order; lane k < K
@@ -90,7 +103,7 @@ __device__ __forceinline__ void warp_select(const float *lg, const uint64_t *__r
     const int lane = threadIdx.x & 31;
     int my_id;
     float my_val;
-    warp_topk<C>(lg, E, K, my_id, my_val);
+    if (warp_topk<C>(lg, E, K, my_id, my_val) && lane == 0) dev_error(ctrl, RL_DEVERR_NAN);
     const float w = topk_weight(my_val, K);
     uint64_t slot = 1;
     if (lane < K) {

@@ -375,7 +375,10 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             if (me < E) {
                 const float lv = fmaf(fixed_value(accv), *scale_s, a.bias ? a.bias[(size_t)l * E + me] : 0.f);
                 key = order_key(lv);
-                if (a.logits_out && blockIdx.x == 0) a.logits_out[(size_t)l * E + me] = lv;
+                if (blockIdx.x == 0) {
+                    if (lv != lv) dev_error(a.ctrl, RL_DEVERR_NAN);
+                    if (a.logits_out) a.logits_out[(size_t)l * E + me] = lv;
+                }
             }
             int my_id;
             float my_val;

@@ -12,6 +12,15 @@ import synth
 REL_F32 = 1e-5        # relative L2 bound of the f32 CUDA-core paths
 REL_BF16 = 5e-3       # relative L2 bound of the bf16 tensor-core path
 W_ABS = 1e-6          # renormalised weights, absolute
+# Router logits against the oracle's f64 logits, relative to the row's largest |logit|.
+# rl_route forms each logit as one f32 dot product (at most a few hundred sequential terms
+# per partial sum), which stays within 1e-6 of the row scale.
+LOGIT_ROUTE = 1e-6
+# moe_decode_stack adds its router partials across CTAs in 64-bit fixed point (2^-36 per CTA
+# partial, then one f32 rounding of the sum and the RMSNorm scale applied to the summed dot),
+# and its layer input is the GPU's own residual stream, which grows with depth; its bound is
+# taken ten times wider.
+LOGIT_FIXED = 1e-5
 
 
 def rel_l2(a, b) -> float:
@@ -54,20 +63,26 @@ class OracleSide:
         return oracle.moe_experts(xn, ids, weights, slots, self.record, self.w.hidden, self.w.inter, self.grid)
 
 
-def check_route(gpu_logits, gpu_ids, gpu_w, gpu_slots, o_logits64, table_row, k, layer, report):
+def check_route(gpu_logits, gpu_ids, gpu_w, gpu_slots, o_logits64, table_row, k, layer, report,
+                logit_tol=LOGIT_ROUTE):
     """Decision protocol for the router.
     (i) the oracle's selection on the GPU's f32 logits equals the GPU's ids and slots
         bit-exactly, weights within W_ABS;
-    (ii) the GPU's logits match the oracle's f64 logits (relative to the row scale);
+    (ii) the GPU's logits match the oracle's f64 logits within logit_tol of the row scale
+        (LOGIT_ROUTE for rl_route, LOGIT_FIXED for the fused stack's fixed-point sums);
     (iii) the oracle's ids from its own logits equal the GPU's, except where two candidates
-        are closer than the measured logit error (a genuine f32 near-tie), which is counted."""
+        are closer than the measured logit error (a genuine f32 near-tie), which is counted in
+        report["near_ties"]; callers bound that count.  report["logit_err"] keeps the largest
+        error seen, relative to the row scale."""
     r = oracle.route_from_logits(gpu_logits, table_row, k, layer)
     assert np.array_equal(r.ids, gpu_ids), "selection on the GPU's logits differs"
     assert np.array_equal(r.slots, gpu_slots), "slot lookup differs"
     assert np.max(np.abs(r.weights - gpu_w)) <= W_ABS, np.max(np.abs(r.weights - gpu_w))
     scale = np.max(np.abs(o_logits64), axis=1, keepdims=True)
     err = np.abs(gpu_logits.astype(np.float64) - o_logits64)
-    assert np.all(err <= 1e-5 * scale), float(np.max(err / scale))
+    rel = float(np.max(err / scale))
+    report["logit_err"] = max(report.get("logit_err", 0.0), rel)
+    assert rel <= logit_tol, (rel, logit_tol)
     own = oracle.select_topk(o_logits64.astype(np.float32), k)
     ties = 0
     for t in np.nonzero(np.any(own != gpu_ids, axis=1))[0]:

@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 import oracle  # noqa: E402
 import synth  # noqa: E402
-from tests._gpu_common import REL_BF16, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
+from tests._gpu_common import LOGIT_FIXED, REL_BF16, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
 
 TINY = synth.WORKLOADS["tiny"]
 DEGENERATE = {
@@ -134,5 +134,40 @@ def test_degenerate_routing_fused_stack(name):
             xn = oracle.rmsnorm(H[l:l + 1])
             r = check_route(b.logits[l:l + 1].cpu().numpy(), b.ids[l:l + 1].cpu().numpy(),
                             b.weights[l:l + 1].cpu().numpy(), u64(b.slots[l:l + 1]),
-                            oracle.router_logits(xn, o.router(l)), o.table_row(l), w.top_k, l, {})
+                            oracle.router_logits(xn, o.router(l)), o.table_row(l), w.top_k, l, {},
+                            logit_tol=LOGIT_FIXED)
             assert rel_l2(H[l + 1] - H[l], o.experts(xn, r.ids, r.weights, r.slots)[0]) <= REL_F32, (t, l)
+
+
+def test_nan_router_logit_is_flagged():
+    """A NaN router logit is refused through RL_DEVERR_NAN in ctrl[1]: it ranks below every
+    number, so the selection is the oracle's top-k over the other logits.  In the fused stack
+    the NaN partial dot is outside the fixed-point range and raises RL_DEVERR_RANGE instead."""
+    engine = _engine()
+    from quantized_moe_expert_rl_gb300 import _lib
+    w = synth.WORKLOADS["tiny"]
+    m = engine.Model(w)
+    m.routers[0][3].fill_(float("nan"))
+    x = torch.from_numpy(synth.tokens(w)).cuda()
+    # decode (rl_route, one token)
+    b = engine.DecodeBuffers.make(m)
+    y = torch.zeros_like(x)
+    engine.enqueue_decode_token(m, b, x[0], y[0], stacked=False, keep_logits=True)
+    torch.cuda.synchronize()
+    lg = b.logits[0].cpu().numpy()
+    assert np.isnan(lg[3]) and int(b.ctrl[1]) & _lib.RL_DEVERR_NAN
+    ref = oracle.select_topk(np.where(np.isnan(lg), -np.inf, lg)[None, :], w.top_k)[0]
+    assert np.array_equal(b.ids[0].cpu().numpy(), ref) and 3 not in ref.tolist()
+    # prefill routing of the chunk
+    bp = engine.PrefillBuffers.make(m, w.tokens)
+    engine.enqueue_prefill_route(m, bp, 0, x, stacked=False, keep_logits=True)
+    torch.cuda.synchronize()
+    lgp = bp.logits.cpu().numpy()
+    assert int(bp.ctrl[1]) & _lib.RL_DEVERR_NAN
+    refp = oracle.select_topk(np.where(np.isnan(lgp), -np.inf, lgp), w.top_k)
+    assert np.array_equal(bp.ids.cpu().numpy(), refp)
+    # the fused stack
+    bf = engine.DecodeBuffers.make(m)
+    engine.enqueue_decode_token_fused(m, bf, x[0], y[1])
+    torch.cuda.synchronize()
+    assert int(bf.ctrl[1]) & _lib.RL_DEVERR_RANGE and not int(bf.ctrl[1]) & _lib.RL_DEVERR_WAIT_TIMEOUT

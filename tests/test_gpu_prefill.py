@@ -51,11 +51,12 @@ def test_prefill_chunk(chunk_model, path, tol):
     assert np.array_equal(b.offs.cpu().numpy().astype(np.uint32), offs)
     assert np.array_equal(b.pair_tok[:P].cpu().numpy().astype(np.uint32), ptok)
     assert np.array_equal(b.pair_k[:P].cpu().numpy(), pk)
-    sample = np.arange(0, T, 16)
-    y_o = o.experts(xo[sample], r.ids[sample], r.weights[sample], r.slots[sample])
-    err = rel_l2(y.cpu().numpy()[sample], y_o)
-    print(f"prefill_chunk {path}: rel L2 {err:.2e} over {len(sample)} tokens, near ties {rep.get('near_ties', 0)}")
+    y_o = o.experts(xo, r.ids, r.weights, r.slots)           # every token of the chunk
+    err = rel_l2(y.cpu().numpy(), y_o)
+    print(f"prefill_chunk {path}: rel L2 {err:.2e} over {T} tokens, logit err {rep['logit_err']:.2e}, "
+          f"near ties {rep.get('near_ties', 0)}")
     assert err <= tol
+    assert rep.get("near_ties", 0) <= 1
 
 
 def test_prefill_paths_agree(chunk_model):
@@ -135,7 +136,10 @@ def test_prefill_bounded(bounded_model, path, tol):
             err = rel_l2(X[l + 1][sample_t] - X[l][sample_t], y_o)
             worst = max(worst, err)
             assert err <= tol, (l, err)
-    print(f"bounded {path}: worst sampled-layer rel L2 {worst:.2e}; near ties {rep.get('near_ties', 0)}")
+    print(f"bounded {path}: worst sampled-layer rel L2 {worst:.2e}; logit err {rep['logit_err']:.2e}; "
+          f"near ties {rep.get('near_ties', 0)}")
+    # a near tie needs two logits within a few 1e-7 of each other: rare among 98k routings
+    assert rep.get("near_ties", 0) <= Lh * T // 1000
 
 
 def test_prefill_bounded_device_fill(bounded_model):

@@ -8,7 +8,7 @@ pytestmark = pytest.mark.gpu
 
 import oracle  # noqa: E402
 import synth  # noqa: E402
-from tests._gpu_common import REL_F32, W_ABS, OracleSide, check_route, rel_l2, u64  # noqa: E402
+from tests._gpu_common import REL_BF16, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -55,14 +55,15 @@ def test_prefill_chunk(tiny, path):
     assert int(b.ctrl[1]) == 0
     xo = x.double().cpu().numpy()
     lg64 = oracle.router_logits(xo, o.router(0))
+    rep = {}
     r = check_route(b.logits.cpu().numpy(), b.ids.cpu().numpy(), b.weights.cpu().numpy(), u64(b.slots), lg64,
-                    o.table_row(0), w.top_k, 0, {})
+                    o.table_row(0), w.top_k, 0, rep)
+    assert rep.get("near_ties", 0) == 0
     offs, ptok, pk = oracle.build_pairs(r.ids, w.n_experts)
     assert np.array_equal(b.offs.cpu().numpy().astype(np.uint32), offs)
     P = T * w.top_k
     assert np.array_equal(b.pair_tok[:P].cpu().numpy().astype(np.uint32), ptok)
     assert np.array_equal(b.pair_k[:P].cpu().numpy(), pk)
     y_o = o.experts(xo, r.ids, r.weights, r.slots)
-    tol = REL_F32 if path == "f32" else 5e-3
+    tol = REL_F32 if path == "f32" else REL_BF16
     assert rel_l2(y.cpu().numpy(), y_o) <= tol
-    assert W_ABS > 0

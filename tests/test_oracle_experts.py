@@ -190,3 +190,134 @@ def test_stack_early_out_and_fill():
     assert np.array_equal(part.x_out, full.x_out)      # the filled chain completes identically
     # brute force: first early-out layer = first layer with a miss
     assert part.first_early_out == min(l for l in range(L) if part.miss[l] > 0)
+
+
+# ----------------------------------------------------------------------------------------------
+# The stack recurrence x_{l+1} = x_l + MoE_l(RMSNorm(x_l)), pinned by a closed form.
+# Every matrix of every expert is constant (an all-8 codebook row, one scale, one sign for the
+# whole matrix) and x starts constant, so x stays a constant vector s_l * 1 and each layer can
+# be written out by hand:
+#   xn     = s / sqrt(s^2 + eps)                  (RMSNorm of a constant vector)
+#   logit_e = r_le * xn   (router rows constant r_le / H), rounded to f32 as the router is
+#   top-K by logit; w_k = exp(l_k - l_1) / sum_j exp(l_j - l_1)
+#   gate = a_e H xn, up = b_e H xn, h = silu(gate) up, o_e = c_e I h
+#   s_{l+1} = s_l + sum_k w_k o_{id_k}
+# A dropped residual, a norm taken after the router or not at all, swapped gate/up, a wrong
+# selection direction or weights from the wrong logits each change s_{l+1}.
+# ----------------------------------------------------------------------------------------------
+def _matrix_blocks(n_blocks, d_bits, negative):
+    blk = bytes([d_bits & 0xFF, d_bits >> 8]) + bytes([0, 0xFF if negative else 0]) * 32
+    return blk * n_blocks
+
+
+def _fp16_pow2(bits):
+    return 2.0 ** (((bits >> 10) & 31) - 15)
+
+
+def _stack_closed_form(x0, routers, experts, K, H, I, eps):
+    """s_l by hand for constant x; routers[l][e] = r_le; experts[l][e] = (a, b, c) values."""
+    s = x0
+    out = [s]
+    sel = []
+    for l in range(len(routers)):
+        xn = s / math.sqrt(s * s + eps)
+        lg = [float(np.float32(r * xn)) for r in routers[l]]
+        order = sorted(range(len(lg)), key=lambda e: (-lg[e], e))[:K]
+        ex = [math.exp(lg[e] - lg[order[0]]) for e in order]
+        tot = 0.0
+        for v in ex:
+            tot += v
+        y = 0.0
+        for j, e in enumerate(order):
+            a, b, c = experts[l][e]
+            g, u = a * H * xn, b * H * xn
+            h = g / (1 + math.exp(-g)) * u
+            y += (ex[j] / tot) * (c * I * h)
+        s = s + y
+        out.append(s)
+        sel.append(order)
+    return out, sel
+
+
+def _stack_case(x0, routers, specs, K, H=256, I=256, eps=1e-6):
+    grid = np.full((256, 8), 8, dtype=np.int8)
+    L, E = len(routers), len(routers[0])
+    nb = H * I // 256
+    recs, vals, layers = {}, [], []
+    for l in range(L):
+        row = np.zeros(E, dtype=np.uint64)
+        vl = []
+        for e in range(E):
+            mats = specs[l][e]           # ((d_bits, negative) for gate, up, down)
+            recs[(l * E + e + 1) * 4096] = np.frombuffer(b"".join(_matrix_blocks(nb, *m) for m in mats),
+                                                         dtype=np.uint8)
+            row[e] = (l * E + e + 1) * 4096
+            vl.append(tuple(8 * _fp16_pow2(db) * (-1.0 if neg else 1.0) for db, neg in mats))
+        vals.append(vl)
+        wr = np.repeat(np.asarray(routers[l], dtype=np.float32)[:, None] / np.float32(H), H, axis=1)
+        layers.append(oracle.LayerInputs(wr, row))
+    x = np.full((1, H), x0)
+    res = oracle.moe_stack(x, layers, K, recs.__getitem__, H, I, grid, eps=eps)
+    expect, sel = _stack_closed_form(x0, routers, vals, K, H, I, eps)
+    return res, expect, sel
+
+
+def test_stack_recurrence_closed_form():
+    # fp16 scales: 0x2000 = 2^-7, 0x1C00 = 2^-8, 0x1800 = 2^-9, 0x1400 = 2^-10, 0x0C00 = 2^-12
+    routers = [[0.75, 0.5, -0.25, -0.5],      # x > 0: layer 0 picks experts 0, 1
+               [-0.5, 0.25, 0.5, 1.0],        # layer 1 picks 3, 2 while x > 0
+               [0.125, -1.0, 0.5, -0.75]]     # the sign of x decides layer 2
+    specs = [
+        [((0x1C00, False), (0x1800, False), (0x0C00, True)), ((0x1800, False), (0x1C00, True), (0x0C00, False)),
+         ((0x1400, False), (0x1400, False), (0x0C00, False)), ((0x1400, True), (0x1400, False), (0x0C00, False))],
+        [((0x1800, False), (0x1800, False), (0x0C00, False)), ((0x1400, False), (0x1800, False), (0x0C00, True)),
+         ((0x1C00, True), (0x1800, False), (0x0C00, False)), ((0x1800, False), (0x1C00, False), (0x0C00, True))],
+        [((0x1800, False), (0x1400, False), (0x0C00, False)), ((0x1C00, False), (0x1800, True), (0x0C00, True)),
+         ((0x1400, False), (0x1C00, False), (0x0C00, True)), ((0x1800, True), (0x1800, False), (0x0C00, False))],
+    ]
+    for x0 in (0.75, -2.0):
+        res, expect, sel = _stack_case(x0, routers, specs, K=2)
+        assert [r.ids[0].tolist() for r in res.routes] == sel
+        for l, xi in enumerate(res.x_in):
+            assert np.allclose(xi, expect[l], rtol=1e-12, atol=0), (x0, l)
+        assert np.allclose(res.x_out, expect[-1], rtol=1e-12, atol=0)
+        # the state moves by more than the tolerance every layer, and not by the MoE term alone
+        for l in range(3):
+            assert abs(expect[l + 1] - expect[l]) > 1e-6 * abs(expect[l + 1])
+            assert abs(expect[l + 1] - (expect[l + 1] - expect[l])) > 1e-3
+    # the two starting signs route layer 0 differently, and some later layer selects other experts
+    r_pos = _stack_case(0.75, routers, specs, K=2)[2]
+    r_neg = _stack_case(-2.0, routers, specs, K=2)[2]
+    assert r_pos[0] != r_neg[0]
+    assert len({tuple(s) for s in r_pos}) >= 2 and len({tuple(s) for s in r_neg}) >= 2
+
+
+def test_stack_closed_form_rejects_planted_mistakes():
+    """The hand-written recurrence above is sensitive to each plausible oracle mistake: the
+    values a mistaken recurrence would give differ from the closed form."""
+    H, I, eps = 256, 256, 1e-6
+    routers = [[0.75, 0.5, -0.25, -0.5], [-0.5, 0.25, 0.5, 1.0]]
+    vals = [[(2 ** -5, 2 ** -6, -(2 ** -9)), (2 ** -6, -(2 ** -5), 2 ** -9), (2 ** -7, 2 ** -7, 2 ** -9),
+             (-(2 ** -7), 2 ** -7, 2 ** -9)]] * 2
+    good, _ = _stack_closed_form(0.75, routers, vals, 2, H, I, eps)
+
+    def variant(residual=True, norm=True, swap=False):
+        s = 0.75
+        for l in range(2):
+            xn = s / math.sqrt(s * s + eps) if norm else s
+            lg = [float(np.float32(r * xn)) for r in routers[l]]
+            order = sorted(range(4), key=lambda e: (-lg[e], e))[:2]
+            ex = [math.exp(lg[e] - lg[order[0]]) for e in order]
+            y = 0.0
+            for j, e in enumerate(order):
+                a, b, c = vals[l][e]
+                if swap:
+                    a, b = b, a
+                g, u = a * H * xn, b * H * xn
+                y += ex[j] / sum(ex) * (c * I * g / (1 + math.exp(-g)) * u)
+            s = s + y if residual else y
+        return s
+
+    assert math.isclose(variant(), good[-1], rel_tol=1e-13)
+    for bad in (variant(residual=False), variant(norm=False), variant(swap=True)):
+        assert not math.isclose(bad, good[-1], rel_tol=1e-6)

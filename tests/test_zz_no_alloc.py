@@ -38,8 +38,11 @@ def test_static_scratch_matches_workspace_entry_point():
         a, r = y_st.double().cpu().numpy(), y_ws.double().cpu().numpy()
         assert rel_l2(a, r) <= REL_F32
         assert np.array_equal(a, r)            # the same kernels run; only the scratch differs
-    # sizes beyond the fixed scratch are refused with a message, before any launch
+    # top_k * inter beyond the fixed scratch is refused before any launch.  Every supported
+    # shape fits the array (the library asserts it at compile time), so the refusal comes from
+    # the shape check that all entry points share.
     big = L.RlShape.of(2048, 512, 16, 2048, 1)
     with pytest.raises(L.RlError) as ei:
         L.moe_decode_static(big, 0, x[0], -1.0, b.slots[0], b.weights[0], m.codebook, x[1], 0, b.ctrl)
     assert ei.value.status == L.RL_ERR_UNSUPPORTED
+    assert "top_k*inter" in str(ei.value)

@@ -46,7 +46,8 @@ def _peaks():
 
 
 def _tensor_peak():
-    """Dense bf16 tensor-core peak in TFLOP/s: the measured burst figure (the chunk's GEMMs are
+    """Dense 16-bit tensor-core peak in TFLOP/s (f16 and bf16 run at the same dense rate): the
+    measured bf16 burst figure (the chunk's GEMMs are
     timed alone), else the fallback."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -512,7 +513,7 @@ def prefill_leg(dev, steps: int, warmup: int, path: str = "tc"):
             "achieved_gbs": bytes_ / t_ex / 1e9, "peak_gbs": hbm, "frac_hbm": t_hbm / t_ex,
             "achieved_tflops": flops / t_ex / 1e12, "peak_tflops": tf, "frac_tensor": t_tc / t_ex,
             "traffic": _traffic("tc_gemm", 1.0), "peak_source": f"{hbm_kind} hbm_gbs, {tf_kind}"}
-    return {"workload": "prefill_chunk (1 layer, 512 tokens, 5120 pairs)", "operands": "bf16" if path == "tc" else "f32",
+    return {"workload": "prefill_chunk (1 layer, 512 tokens, 5120 pairs)", "operands": "f16" if path == "tc" else "f32",
             "roofline": roof,
             "tokens_per_s": T / (res["path"] * 1e-3), "ms_per_chunk": res["path"],
             "experts_ms_per_chunk": res["experts"], "experts_tokens_per_s": T / t_ex,

@@ -293,7 +293,11 @@ rl_status rl_build_pairs(const rl_moe_shape *shp, int32_t layer, int32_t T, cons
  * each token's top-k accumulated in router selection order):
  *   y[t][h] = (accumulate ? y[t][h] : 0) + sum_{k in order} weights[t][k] * o_{t,k}[h].
  * Gate/up and down run as grouped GEMMs on the 5th-generation tensor cores (tcgen05,
- * accumulators in tensor memory) with both operands rounded to bf16 and f32 accumulation.
+ * accumulators in tensor memory) with 16-bit operands and f32 accumulation: the weights are
+ * decoded to IEEE half precision (d * codebook value * sign, rounded once) straight into tensor
+ * memory, the activations x and h are rounded to half precision (|x|, |h| must stay below
+ * 65504).  Half precision keeps 11 significant bits against bfloat16's 8: with both operands
+ * rounded, bfloat16 left the chunk's relative error near 3e-3 of a 5e-3 budget.
  * xn [T][H] f32; offs/pair_tok/pair_k from rl_build_pairs; slots uint64 [T][K] and weights
  * f32 [T][K] from rl_route; codebook int8 [256][8]; y [T][H] f32.  Skip when
  * ctrl[0] <= layer.  ws: moe_prefill_workspace_bytes(shp, T) bytes.

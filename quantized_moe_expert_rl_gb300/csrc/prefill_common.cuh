@@ -1,5 +1,5 @@
 // prefill_common.cuh - argument checks, workspace layout and the ordered combine shared by
-// the two grouped prefill paths (tensor-core bf16 and CUDA-core f32).
+// the two grouped prefill paths (tensor-core f16 and CUDA-core f32).
 #pragma once
 #include "rl_common.cuh"
 
@@ -16,23 +16,24 @@ struct PrefillArgs {
     float *y;
     int32_t *ctrl;
     // workspace carve-up
-    float *hbuf;              // [P][I]   f32 SwiGLU activations, pair order
+    float *hbuf;              // [P][I]   f32 SwiGLU activations, pair order (f32 path)
     float *outbuf;            // [T*K][H] f32 expert outputs, indexed by (token, k)
-    uint16_t *xb16;           // [T][H]   16-bit copy of xn (tensor-core path)
-    uint16_t *hb16;           // [P][I]   16-bit SwiGLU activations, pair order (tensor-core path)
+    uint16_t *xb16;           // [P'][H]  f16 copy of xn gathered in pair order (tensor-core path)
+    uint16_t *hb16;           // [P'][I]  f16 SwiGLU activations, pair order (tensor-core path)
     void *units;              // tensor-core work-unit lists
 };
 
+// P' = max(P, 16): the tensor-core path reads its 16-bit operands in boxes of 16 pair rows
 struct PrefillWs {
     size_t h, out, xb, hb, units, total;
     PrefillWs(int T, int H, int K, int I, int E) {
-        const size_t P = (size_t)T * K;
+        const size_t P = (size_t)T * K, P16 = P > 16 ? P : 16;
         h = align_up(P * I * sizeof(float), 256);
         out = align_up(P * H * sizeof(float), 256);
-        xb = align_up((size_t)T * H * 2, 256);
-        hb = align_up(P * I * 2, 256);
-        // unit lists: at most (P / 32 + E) token blocks x (I / 64 gate/up + H / 128 down) row tiles
-        units = align_up(256 + 4 * (P / 32 + (size_t)E) * ((size_t)I / 64 + (size_t)H / 128), 256);
+        xb = align_up(P16 * H * 2, 256);
+        hb = align_up(P16 * I * 2, 256);
+        // unit lists: at most (P / 128 + E) token blocks x (I / 64 gate/up + H / 128 down) row tiles
+        units = align_up(256 + 4 * (P / 128 + (size_t)E) * ((size_t)I / 64 + (size_t)H / 128), 256);
         total = h + out + xb + hb + units;
     }
 };

@@ -2,27 +2,26 @@
 //
 // Red Lite dev20 - batched prompt ingestion, "What changed" item 3: the chunk's routed experts
 // run as batched gate/up and down over (expert, token) pairs sorted by expert, then each
-// token's top-k outputs are accumulated in router selection order.  Section "dev20d: expert
-// kernel layout" decodes each block one 8-value group at a time on another GPU; here the
-// decoded weights feed the 5th-generation tensor cores:
+// token's top-k outputs are accumulated in router selection order; a plan covers at most the
+// 512 experts of a layer.  Section "dev20d: expert kernel layout" decodes each block one
+// 8-value group at a time on another GPU; here the decoded weights feed the 5th-generation
+// tensor cores:
 //
-//   unit = (expert e, token block of <= 128 of its pairs, row tile); one CTA per SM walks the
-//   device-built unit list.  Per unit:
-//     - one elected thread bulk-copies the unit's quantized weight rows into shared memory
-//       (gate/up tile: 64 gate rows + the same 64 up rows, so SwiGLU pairs stay in the CTA;
-//       down tile: 128 rows);
-//     - K is streamed in chunks of 64: every thread decodes its share of the 128 x 64 A chunk
-//       (codebook value with its sign, WITHOUT the block scale: the values are small integers,
-//       exact in 16 bits) straight into the canonical K-major core-matrix layout, while
-//       cp.async gathers the matching 64 columns of the unit's token rows (B) two chunks ahead;
-//     - one thread issues tcgen05.mma (M = 128, N = tokens rounded to 16, K = 16 x 4) into a
-//       separate f32 tensor-memory accumulator per 256-value block of the row, and commits to
-//       the stage's mbarrier;
-//     - epilogue: tcgen05.ld -> registers; the block scales are applied in f32,
-//       D[m][n] = sum_b d[m][b] * D_b[m][n]; then h = silu(g) * u (16-bit, pair order) for
-//       gate/up, or the f32 per-pair outputs of down, indexed by (token, k) for the combine.
-// So the only 16-bit roundings are the activations (x, h).  Operand type T16 is bf16 (the
-// default) or f16; both operands of one MMA share it.
+//   unit = (expert e, token block of <= 128 of its pairs, row tile of 128 weight rows).  The
+//   A operand (weights) is decoded from the quantized rows straight into TENSOR MEMORY by the
+//   producer warps (tcgen05.st: lane m = weight row m), so the decoded weights never pass
+//   through shared memory; the B operand (the unit's activations, 16-bit, pair order) arrives
+//   by TMA tensor copies with the 128-byte swizzle; one thread issues
+//   tcgen05.mma (A from tensor memory, B from shared memory, f32 accumulator in tensor memory).
+//
+// Operands are IEEE half precision: a weight is d * codebook[idx][j] * (+-1) rounded once to
+// f16 (the product of the f16 scale and the small integer needs up to 17 bits; f16 keeps 11),
+// the activations x and h are rounded to f16.  The f32 accumulator sees every K term.
+//
+// Weights are the same for every token of a unit, so a heavy expert (many tokens, the Zipf
+// head of a skewed chunk) decodes its rows once per 128 tokens; the unit list puts the full
+// 128-token blocks first and the work is taken from a global counter, so the heavy units start
+// first and the light ones fill in behind them.
 #include <algorithm>
 
 #include "prefill_common.cuh"
@@ -31,42 +30,37 @@
 
 namespace rl {
 
-constexpr int kNT = 128;         // max tokens per unit
-#ifndef RL_TC_KC
-#define RL_TC_KC 64
-#endif
-constexpr int kKC = RL_TC_KC;    // K elements per chunk
-constexpr int kKG = kKC / 8;     // 16-byte core-matrix columns (8 values) per chunk
+constexpr int kNT = 128;        // tokens (pairs) per unit, the MMA's N at most
+constexpr int kTcRows = 128;    // weight rows per unit: the MMA's M (gate/up: 64 gate + 64 up rows)
+constexpr int kGuUnits = 64;    // hidden units per gate/up unit
+constexpr int kStepV = 128;     // K values per A stage in tensor memory (half a 256-value block)
+constexpr int kAStages = 4;     // A stages: producer set J fills stages J and J + 2 in turn
+constexpr int kChunkV = 64;     // K values per B chunk (one 128-byte swizzle row of f16)
 
-// accumulators (256-value blocks) per row of length C
-__host__ __device__ inline int tc_nblk(int C) { return C >= 256 ? C / 256 : 1; }
-constexpr int kGuRows = 64;      // gate rows (and up rows) per gate/up unit
-constexpr int kDnRowsTc = 128;   // down rows per down unit
+// warp roles
+constexpr int kTcProd = 8;                  // 0-7: A producers, two sets of four lane quadrants
+constexpr int kTcMmaW = 8;                  // MMA issuer (lane 0)
+constexpr int kTcRawW = 9;                  // unit fetch, pair metadata, bulk copy of the quantized rows
+constexpr int kTcBW = 10;                   // B tensor copies (lane 0)
+constexpr int kTcEpi0 = 11;                 // 11-14: epilogue, lane quadrants 3, 0, 1, 2
+constexpr int kTcWarps = 15;
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kRawArrivals = kTcProd + 1 + 1 + 4;  // every role that reads a unit's metadata
 
-template <typename T16>
-struct TcType;
-template <>
-struct TcType<__nv_bfloat16> {
-    static constexpr uint32_t fmt = 1;
-    __device__ static uint32_t bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
-    __device__ static uint32_t mul2(uint32_t a, uint32_t b) {
-        __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
-        return *reinterpret_cast<uint32_t *>(&r);
-    }
-};
-template <>
-struct TcType<__half> {
-    static constexpr uint32_t fmt = 0;
-    __device__ static uint32_t bits(float v) { return __half_as_ushort(__float2half_rn(v)); }
-    __device__ static uint32_t mul2(uint32_t a, uint32_t b) {
-        __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
-        return *reinterpret_cast<uint32_t *>(&r);
-    }
-};
+// tensor memory: A stages at columns [0, 256) (64 columns each), accumulators at [256, 512)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol0 = 256;
 
-// codebook as 16-bit pairs of type T16, 8 interleaved copies (see qdot.cuh)
-template <typename T16>
-__device__ void build_pair_table_t(uint4 *tab, const int8_t *__restrict__ codebook) {
+// B stages of kNT rows x 128 bytes; a unit of npad tokens packs cps = 128 / npad chunks (a power
+// of two) into one stage, so that small units keep as many K values in flight as large ones
+__host__ __device__ inline int tc_bstages(int MODE) { return MODE == 0 ? 3 : 6; }
+__host__ __device__ inline int tc_cps(int npad, int nchunks) {
+    int c = 1;
+    while (2 * c * npad <= kNT && 2 * c <= nchunks) c *= 2;
+    return c;
+}
+// codebook as f16 pairs (exact: |value| <= 128), 8 interleaved copies (see qdot.cuh)
+__device__ void build_pair_table_f16(uint4 *tab, const int8_t *__restrict__ codebook) {
     for (int e = threadIdx.x; e < 256; e += blockDim.x) {
         const uint2 raw = reinterpret_cast<const uint2 *>(codebook)[e];
         uint32_t w[4];
@@ -75,7 +69,7 @@ __device__ void build_pair_table_t(uint4 *tab, const int8_t *__restrict__ codebo
             const uint32_t word = p < 2 ? raw.x : raw.y;
             const int g0 = (int8_t)((word >> (16 * (p & 1))) & 0xffu);
             const int g1 = (int8_t)((word >> (16 * (p & 1) + 8)) & 0xffu);
-            w[p] = TcType<T16>::bits((float)g0) | (TcType<T16>::bits((float)g1) << 16);
+            w[p] = (uint32_t)__half_as_ushort(__int2half_rn(g0)) | ((uint32_t)__half_as_ushort(__int2half_rn(g1)) << 16);
         }
         const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
 #pragma unroll
@@ -83,16 +77,16 @@ __device__ void build_pair_table_t(uint4 *tab, const int8_t *__restrict__ codebo
     }
 }
 
-struct TcUnits {   // unit lists in the workspace: [count_gu, count_dn, pad..][gu units][dn units]
-    uint32_t *counts, *gu, *dn;
-    size_t max_gu, max_dn;
-};
-
-__host__ __device__ inline size_t tc_max_units(int P, int E, int nt, int per_block) {
-    return ((size_t)P / nt + E) * per_block;
+// ---- unit lists ------------------------------------------------------------------------------
+// A unit word: expert (bits 0-9), row tile (10-14), token block (15-31).
+__host__ __device__ inline uint32_t unit_word(int e, int mt, int tb) {
+    return (uint32_t)e | ((uint32_t)mt << 10) | ((uint32_t)tb << 15);
 }
+struct TcUnits {  // [count_gu, count_dn, next_gu, next_dn, pad..][gu units][dn units]
+    uint32_t *counts, *gu, *dn;
+};
+__host__ __device__ inline size_t tc_max_blocks(int P, int E) { return (size_t)P / kNT + (size_t)E; }
 
-// ---- unit lists: per expert ceil(n_e / kNT) token blocks x row tiles -------------------------
 // block-wide exclusive scan of one value per thread (blockDim <= 512); returns (prefix, total)
 __device__ __forceinline__ uint2 block_scan512(uint32_t v, uint32_t *scan_s) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -113,179 +107,228 @@ __device__ __forceinline__ uint2 block_scan512(uint32_t v, uint32_t *scan_s) {
     return make_uint2(base + incl - v, total);
 }
 
-// unit = (expert, token block, row tile); token blocks of nt_gu (gate/up) and nt_dn (down)
-__global__ void __launch_bounds__(512) tc_units_kernel(const uint32_t *__restrict__ offs, int E, int nt_gu,
-                                                       int gu_tiles, int nt_dn, int dn_tiles, uint32_t *counts,
-                                                       uint32_t *gu, uint32_t *dn, const int32_t *ctrl, int layer) {
+// Per expert: its full 128-pair blocks first (all experts), then its partial block; each block
+// times the row tiles of the mode.  Zeroes the two work counters.
+__global__ void __launch_bounds__(512) tc_units_kernel(const uint32_t *__restrict__ offs, int E, int gu_tiles,
+                                                       int dn_tiles, uint32_t *counts, uint32_t *gu, uint32_t *dn,
+                                                       const int32_t *ctrl, int layer) {
     __shared__ uint32_t scan_s[16];
     if (ld_ctrl(ctrl) <= layer) return;
     const int e = threadIdx.x;
     const uint32_t n = e < E ? offs[e + 1] - offs[e] : 0u;
-    const uint32_t nbg = (n + nt_gu - 1) / nt_gu, nbd = (n + nt_dn - 1) / nt_dn;
-    const uint2 sg = block_scan512(nbg, scan_s);
-    const uint2 sd = block_scan512(nbd, scan_s);
-    for (uint32_t tb = 0; tb < nbg; ++tb)
-        for (int mt = 0; mt < gu_tiles; ++mt) gu[(sg.x + tb) * gu_tiles + mt] = e | (tb << 10) | ((uint32_t)mt << 20);
-    for (uint32_t tb = 0; tb < nbd; ++tb)
-        for (int mt = 0; mt < dn_tiles; ++mt) dn[(sd.x + tb) * dn_tiles + mt] = e | (tb << 10) | ((uint32_t)mt << 20);
+    const uint32_t full = n / kNT, part = (n % kNT) ? 1u : 0u;
+    const uint2 sf = block_scan512(full, scan_s);
+    const uint2 sp = block_scan512(part, scan_s);
+    for (uint32_t f = 0; f < full; ++f) {
+        for (int mt = 0; mt < gu_tiles; ++mt) gu[(size_t)(sf.x + f) * gu_tiles + mt] = unit_word(e, mt, (int)f);
+        for (int mt = 0; mt < dn_tiles; ++mt) dn[(size_t)(sf.x + f) * dn_tiles + mt] = unit_word(e, mt, (int)f);
+    }
+    if (part) {
+        for (int mt = 0; mt < gu_tiles; ++mt) gu[(size_t)(sf.y + sp.x) * gu_tiles + mt] = unit_word(e, mt, (int)full);
+        for (int mt = 0; mt < dn_tiles; ++mt) dn[(size_t)(sf.y + sp.x) * dn_tiles + mt] = unit_word(e, mt, (int)full);
+    }
     if (e == 0) {
-        counts[0] = sg.y * gu_tiles;
-        counts[1] = sd.y * dn_tiles;
+        counts[0] = (sf.y + sp.y) * gu_tiles;
+        counts[1] = (sf.y + sp.y) * dn_tiles;
+        counts[2] = 0u;
+        counts[3] = 0u;
     }
 }
 
-template <typename T16>
-__global__ void __launch_bounds__(256) tc_convert_kernel(const float *__restrict__ x, uint16_t *__restrict__ xb,
-                                                         size_t n, const int32_t *ctrl, int layer) {
+// xg[p][:] = f16(xn[pair_tok[p]][:]): the gate/up B operand in pair order, one warp per pair
+__global__ void __launch_bounds__(256) tc_gather_kernel(const float *__restrict__ xn,
+                                                        const uint32_t *__restrict__ pair_tok,
+                                                        uint16_t *__restrict__ xg, int P, int H, const int32_t *ctrl,
+                                                        int layer) {
     if (ld_ctrl(ctrl) <= layer) return;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        xb[i] = (uint16_t)TcType<T16>::bits(x[i]);
+    const int lane = threadIdx.x & 31;
+    const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (p >= P) return;
+    const float4 *src = reinterpret_cast<const float4 *>(xn + (size_t)pair_tok[p] * H);
+    uint4 *dst = reinterpret_cast<uint4 *>(xg + (size_t)p * H);
+    for (int c = lane; c < H / 8; c += 32) {
+        const float4 a = __ldg(src + 2 * c), b = __ldg(src + 2 * c + 1);
+        const __half2 h0 = __floats2half2_rn(a.x, a.y), h1 = __floats2half2_rn(a.z, a.w);
+        const __half2 h2 = __floats2half2_rn(b.x, b.y), h3 = __floats2half2_rn(b.z, b.w);
+        dst[c] = make_uint4(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
+                            *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
+    }
 }
 
-// ---- the grouped GEMM: a warp-specialised pipeline -------------------------------------------
-// Warp roles (18 warps):
-//   0-11  producers: for every 64-wide K chunk of a unit, gather the unit's token rows of the
-//         B operand (16-bit activations) and decode the 128 x 64 A chunk from the quantized rows
-//         into one stage of a ring (canonical K-major core-matrix layout), then arrive on the
-//         stage's "full" barrier;
-//   12    MMA issuer (lane 0): per chunk, waits "full", issues the tcgen05.mma of the chunk into
-//         the unit's tensor-memory accumulators and commits to the stage's "empty" barrier;
-//         after a unit's last chunk, commits to the accumulator's "full" barrier;
-//   13    loader: stages the next unit's token list and bulk-copies its quantized rows into the
-//         other of two raw buffers;
-//   14-17 epilogue: the four TMEM lane quadrants (warp w reads lanes 32 (w % 4) ...); applies the
-//         block scales and writes h (gate/up) or the per-pair outputs (down), then releases the
-//         accumulator and the raw buffer.
-// The accumulators (one per 256-value block, nt tokens wide) are double-buffered in tensor
-// memory, so a unit's epilogue overlaps the next unit's MMAs; the raw rows are double-buffered
-// so the next unit's copy overlaps the current unit.  Every wait is bounded; a timeout sets a
-// shared abort flag and every role leaves its loop.
-constexpr int kTcProducers = 12;
-constexpr int kTcMmaWarp = 12;
-constexpr int kTcLoadWarp = 13;
-constexpr int kTcEpiWarp0 = 14;
-constexpr int kTcThreads2 = 18 * 32;
-constexpr int kTcPT = kTcProducers * 32;              // producer threads
-constexpr int kTcBMax = (kNT * kKG + kTcPT - 1) / kTcPT;  // B pieces per producer thread and chunk
-constexpr int kTcAItems = (128 * kKG + kTcPT - 1) / kTcPT;
-#ifndef RL_TC_STAGES
-#define RL_TC_STAGES 2
-#endif
-constexpr int kTcStages = RL_TC_STAGES;
-
-// tokens per unit when the accumulators are double-buffered: 2 x nblk x nt <= 512 columns
-__host__ __device__ inline int tc_nt2(int C) { return 256 / tc_nblk(C) < kNT ? 256 / tc_nblk(C) : kNT; }
-
-struct TcMeta {        // one unit, staged by the loader
-    int e, mt, nvalid, npad;
+// ---- the grouped GEMM ------------------------------------------------------------------------
+struct TcMeta {  // one unit, staged by the raw loader
+    int end, e, mt, nvalid, npad;
     uint32_t p_lo;
     uint32_t tok[kNT];
-    uint8_t k[kNT];
+    uint8_t kk[kNT];
 };
 
 struct TcLayout {
-    size_t raw, stA, stB, o_meta, o_raw, o_st, o_u, total;
+    size_t rawb, o_tab, o_b, o_meta, o_raw, total;
+    int sb;
     __host__ __device__ TcLayout(int MODE, int H, int I) {
-        raw = align_up(MODE == 0 ? 2 * matrix_bytes(kGuRows, H) : matrix_bytes(kDnRowsTc, I), 128);
-        const int nt = tc_nt2(MODE == 0 ? H : I);
-        stA = 128 * kKC * 2;
-        stB = (size_t)nt * kKC * 2;
-        o_meta = 1024 + kTabBytes;
+        sb = tc_bstages(MODE);
+        rawb = align_up(MODE == 0 ? matrix_bytes(kTcRows, H) : matrix_bytes(kTcRows, I), 128);
+        o_tab = 1024;
+        o_b = o_tab + kTabBytes;  // 1024-aligned: the swizzle atoms
+        o_meta = o_b + (size_t)sb * kNT * kChunkV * 2;
         o_raw = align_up(o_meta + 2 * sizeof(TcMeta), 128);
-        o_st = o_raw + 2 * raw;
-        o_u = o_st + kTcStages * (stA + stB);
-        total = o_u + (MODE == 0 ? (size_t)kGuRows * nt * sizeof(float) : 0);
+        total = o_raw + 2 * rawb;
     }
 };
 
-// MODE 0: gate/up -> hb (16-bit h, pair order).  MODE 1: down -> outbuf (f32, (token, k) order).
-template <typename T16, int MODE>
-__global__ void __launch_bounds__(kTcThreads2, 1) tc_gemm_kernel(PrefillArgs a, TcUnits U) {
+struct TcArgs {
+    CUtensorMap bmap;  // B operand [P][C] f16, box 64 x 16 rows, 128-byte swizzle
+    PrefillArgs a;
+    TcUnits U;
+};
+
+// One 8-value group -> four f16 pairs of d * value from its table entry q (the group's
+// codebook row as f16 pairs): sign bits of gs, then the scale.
+__device__ __forceinline__ void group_f16(uint4 q, uint32_t gs, uint32_t dd, uint32_t *out) {
+    const uint32_t s = (gs >> 8) & 0xffu;
+    const uint32_t s2 = s | ((s << 15) & 0x007f0000u);  // bit 2i -> 15 and 2i+1 -> 31 after << (15 - 2i)
+    const __half2 d2 = *reinterpret_cast<const __half2 *>(&dd);
+    uint32_t w[4] = {q.x ^ ((s2 << 15) & 0x80008000u), q.y ^ ((s2 << 13) & 0x80008000u),
+                     q.z ^ ((s2 << 11) & 0x80008000u), q.w ^ ((s2 << 9) & 0x80008000u)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&w[i]), d2);
+        out[i] = *reinterpret_cast<const uint32_t *>(&v);
+    }
+}
+// 8 groups -> 32 words, the 8 table loads issued before any arithmetic (`tabc` = shared-window
+// address of this lane's copy of the table)
+__device__ __forceinline__ void groups8_f16(const uint32_t (&gs)[8], uint32_t dd, uint32_t tabc, uint32_t (&out)[32]) {
+    uint4 q[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) q[g] = lds128(tabc + (gs[g] & 0xffu) * (16 * kTabCopies));
+#pragma unroll
+    for (int g = 0; g < 8; ++g) group_f16(q[g], gs[g], dd, &out[4 * g]);
+}
+
+// Producer step: `ng` groups from flat group index G0 of the raw tile (shared-window address
+// `raw`; rows of C values stored back to back in 66-byte blocks), d of block G0 >> 5.  Each
+// group index is read with its own 16-bit load: a variant that loaded whole 16-byte pieces of
+// the 528-byte rows and unpacked them from registers needed one unrolled copy per block and
+// half and ran four times slower (instruction-cache misses).
+__device__ __forceinline__ void produce_generic(uint32_t raw, int G0, int ng, uint32_t tabc, uint32_t tcol) {
+    const uint32_t db = lds_u16(raw + (uint32_t)(G0 >> 5) * kBlockBytes);
+    const uint32_t dd = db | (db << 16);
+    for (int pc = 0; pc < ng / 8; ++pc) {
+        uint32_t gs[8], out[32];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const int G = G0 + 8 * pc + g;
+            gs[g] = lds_u16(raw + (uint32_t)(G >> 5) * kBlockBytes + 2 + 2 * (G & 31));
+        }
+        groups8_f16(gs, dd, tabc, out);
+        tc::st32(tcol + 32 * pc, out);
+    }
+}
+
+// MODE 0: gate/up -> hb (f16 h, pair order).  MODE 1: down -> outbuf (f32, (token, k) order).
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs args) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    const PrefillArgs &a = args.a;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *raw_full = bars, *raw_empty = bars + 2;          // [2] each
-    uint64_t *acc_full = bars + 4, *acc_empty = bars + 6;      // [2] each
-    uint64_t *st_full = bars + 8, *st_empty = bars + 8 + kTcStages;
-    uint64_t *fin_bar = bars + 8 + 2 * kTcStages;
-    uint64_t *ex_full = fin_bar + 1, *ex_empty = fin_bar + 2;  // gate/up epilogue: u parked / consumed
-    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(smem + 256);
-    int *abort_s = reinterpret_cast<int *>(smem + 260);
-    uint4 *tab = reinterpret_cast<uint4 *>(smem + 1024);
+    uint64_t *raw_full = bars, *raw_empty = bars + 2, *a_full = bars + 4, *a_empty = bars + 8;
+    uint64_t *acc_full = bars + 12, *acc_empty = bars + 14, *fin_bar = bars + 16;
+    uint64_t *b_full = bars + 24, *b_empty = bars + 40;  // [sb] each, sb <= 16
+    uint32_t *tmem_s = reinterpret_cast<uint32_t *>(smem + 512);
+    int *abort_s = reinterpret_cast<int *>(smem + 516);
     const TcLayout lay(MODE, a.H, a.I);
+    const int SB = lay.sb;
+    uint4 *tab = reinterpret_cast<uint4 *>(smem + lay.o_tab);
+    uint8_t *bst = smem + lay.o_b;  // [SB][kNT rows][128 B]
     TcMeta *meta = reinterpret_cast<TcMeta *>(smem + lay.o_meta);
-    uint8_t *rawb = smem + lay.o_raw;                            // [2][lay.raw]
-    uint8_t *stg = smem + lay.o_st;                              // [kTcStages][stA + stB]
-    float *u_s = reinterpret_cast<float *>(smem + lay.o_u);      // [kGuRows][nt] (gate/up)
+    uint8_t *rawb = smem + lay.o_raw;  // [2][lay.rawb]
 
     if (ld_ctrl(a.ctrl) <= a.layer) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int C = MODE == 0 ? a.H : a.I;  // K of this GEMM (row length)
-    const int nblk = tc_nblk(C), nt = tc_nt2(C);
-    const int nch = C / kKC;
-    const uint32_t acc_cols = (uint32_t)(nblk * nt);  // one accumulator set; two are allocated
+    const int C = MODE == 0 ? a.H : a.I;       // K of this GEMM (row length)
+    const int nsteps = C / kStepV;               // A stages per unit (C >= 128)
+    const int nchunks = C / kChunkV;             // B chunks per unit
     if (tid == 0) {
-        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], (i >= 2 && i < 4) ? kTcProducers + 4 : (i >= 6 ? 4 : 1));
-        for (int i = 0; i < kTcStages; ++i) {
-            mbar_init(&st_full[i], kTcProducers);
-            mbar_init(&st_empty[i], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], kRawArrivals);
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        for (int i = 0; i < kAStages; ++i) {
+            mbar_init(&a_full[i], 4);
+            mbar_init(&a_empty[i], 1);
         }
         mbar_init(fin_bar, 1);
-        mbar_init(ex_full, 2);   // the two up-row warps
-        mbar_init(ex_empty, 2);  // the two gate-row warps
+        for (int i = 0; i < SB; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
+        }
         *abort_s = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tc::tmem_alloc(tmem_s, 512);
+        tc::tmem_alloc(tmem_s, kTmemCols);
         tc::tmem_relinquish();
     }
-    build_pair_table_t<T16>(tab, a.codebook);
+    build_pair_table_f16(tab, a.codebook);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_s;
-    const uint32_t count = __ldcg(&U.counts[MODE]);
-    const uint32_t *units = MODE == 0 ? U.gu : U.dn;
-    const uint32_t nmine = count > blockIdx.x ? (count - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
-    const size_t rowb_q = matrix_bytes(1, a.H);  // bytes of an H-wide row (gate/up)
-    const size_t matb = matrix_bytes(a.I, a.H);
+    const uint32_t count = __ldcg(&args.U.counts[MODE]);
+    const uint32_t *units = MODE == 0 ? args.U.gu : args.U.dn;
     bool failed = false;
-    // whole warp; bounded; sets the abort flag.  The per-chunk hand-offs between producers and
-    // the MMA issuer spin on test_wait (a suspended try_wait wakes too late for them); the
-    // long waits (a whole unit) suspend, so that waiting warps leave the issue slots free.
-    auto wait_spin = [&](uint64_t *bar, uint32_t parity) {
-        if (!mbar_spin_warp(bar, parity)) {
-            if (lane == 0) atomicExch(abort_s, 1);
-            failed = true;
-        }
-        return !failed;
-    };
-    auto wait = [&](uint64_t *bar, uint32_t parity) {
-        if (!mbar_wait_warp(bar, parity)) {
-            if (lane == 0) atomicExch(abort_s, 1);
-            failed = true;
-        }
-        return !failed;
-    };
     auto aborted = [&]() { return *reinterpret_cast<volatile int *>(abort_s) != 0; };
+    auto fail_now = [&]() {
+        if (lane == 0) atomicExch(abort_s, 1);
+        failed = true;
+    };
+    // Bounded waits (whole warp; warp-uniform result): lane 0 polls with test_wait, which never
+    // suspends.  A suspended try_wait wakes up microseconds after the phase completes, which
+    // the unit-level hand-offs (metadata, accumulators) cannot afford either.
+    auto wait_spin = [&](uint64_t *bar, uint32_t parity) {
+        if (!mbar_spin_warp(bar, parity)) fail_now();
+        return !failed;
+    };
+    // unit k's metadata (raw_full of its buffer); NULL at the end of the list or on failure
+    auto next_meta = [&](uint32_t k) -> const TcMeta * {
+        if (aborted() || !wait_spin(&raw_full[k & 1], (k >> 1) & 1)) return nullptr;
+        const TcMeta *m = &meta[k & 1];
+        return m->end ? nullptr : m;
+    };
 
-    if (warp == kTcLoadWarp) {
-        // ---------------- loader ----------------
-        uint32_t issued = 0;
-        for (uint32_t k = 0; k < nmine && !failed && !aborted(); ++k) {
+    if (warp == kTcRawW) {
+        // ---------------- unit fetch + quantized rows ----------------
+        const size_t matb = matrix_bytes(a.I, a.H);
+        uint32_t k = 0;
+        for (;; ++k) {
             const int rb = k & 1;
-            if (k >= 2 && !wait(&raw_empty[rb], ((k >> 1) - 1) & 1)) break;
-            const uint32_t uw = __ldcg(&units[blockIdx.x + k * gridDim.x]);
-            const int e = uw & 1023, tb = (uw >> 10) & 1023, mt = uw >> 20;
-            const uint32_t pe0 = __ldcg(&a.offs[e]), pe1 = __ldcg(&a.offs[e + 1]);
-            const uint32_t p_lo = pe0 + tb * nt;
-            const int nvalid = (int)min((uint32_t)nt, pe1 - p_lo);
+            if (k >= 2 && (aborted() || !wait_spin(&raw_empty[rb], ((k >> 1) - 1) & 1))) break;
+            uint32_t u = 0;
+            if (lane == 0) u = atomicAdd(&args.U.counts[2 + MODE], 1u);
+            u = __shfl_sync(kFull, u, 0);
             TcMeta &m = meta[rb];
+            if (u >= count) {
+                if (lane == 0) m.end = 1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_full[rb]);
+                ++k;  // this buffer's phase completed without a copy
+                break;
+            }
+            const uint32_t uw = __ldcg(&units[u]);
+            const int e = uw & 1023, mt = (uw >> 10) & 31, tb = uw >> 15;
+            const uint32_t pe0 = __ldcg(&a.offs[e]), pe1 = __ldcg(&a.offs[e + 1]);
+            const uint32_t p_lo = pe0 + (uint32_t)tb * kNT;
+            const int nvalid = (int)min((uint32_t)kNT, pe1 - p_lo);
             for (int i = lane; i < nvalid; i += 32) {
                 m.tok[i] = __ldcg(&a.pair_tok[p_lo + i]);
-                m.k[i] = __ldcg(&a.pair_k[p_lo + i]);
+                m.kk[i] = __ldcg(&a.pair_k[p_lo + i]);
             }
             if (lane == 0) {
+                m.end = 0;
                 m.e = e;
                 m.mt = mt;
                 m.nvalid = nvalid;
@@ -294,220 +337,199 @@ __global__ void __launch_bounds__(kTcThreads2, 1) tc_gemm_kernel(PrefillArgs a, 
             }
             __syncwarp();
             if (lane == 0) {
-                const uint64_t slot = __ldcg(&a.slots[(size_t)m.tok[0] * a.K + m.k[0]]);
+                const uint64_t slot = __ldcg(&a.slots[(size_t)m.tok[0] * a.K + m.kk[0]]);
                 if (slot == 0 || (slot & 15)) {
                     // nothing is copied: the unit's outputs are garbage and the host sees the flag
                     dev_error(a.ctrl, slot == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN);
                     mbar_arrive(&raw_full[rb]);
                 } else {
                     const uint8_t *rec = reinterpret_cast<const uint8_t *>(slot);
-                    uint8_t *dst = rawb + rb * lay.raw;
+                    uint8_t *dst = rawb + rb * lay.rawb;
                     if (MODE == 0) {
-                        const uint32_t b = (uint32_t)(kGuRows * rowb_q);
-                        const uint8_t *g = rec + (size_t)mt * kGuRows * rowb_q;
+                        const uint32_t b = (uint32_t)matrix_bytes(kGuUnits, a.H);
+                        const uint8_t *g = rec + (size_t)mt * b;
                         mbar_arrive_expect_tx(&raw_full[rb], 2 * b);
                         bulk_g2s(dst, g, b, &raw_full[rb]);
                         bulk_g2s(dst + b, g + matb, b, &raw_full[rb]);
                     } else {
-                        const uint32_t b = (uint32_t)matrix_bytes(kDnRowsTc, a.I);
+                        const uint32_t b = (uint32_t)matrix_bytes(kTcRows, a.I);
                         mbar_arrive_expect_tx(&raw_full[rb], b);
-                        bulk_g2s(dst, rec + 2 * matb + matrix_bytes(mt * kDnRowsTc, a.I), b, &raw_full[rb]);
+                        bulk_g2s(dst, rec + 2 * matb + (size_t)mt * b, b, &raw_full[rb]);
                     }
                 }
             }
             __syncwarp();
-            issued = k + 1;
         }
-        // every copy this warp issued must have landed before the CTA may exit
-        for (uint32_t k = issued >= 2 ? issued - 2 : 0; k < issued; ++k) mbar_wait_warp(&raw_full[k & 1], (k >> 1) & 1);
-    } else if (warp < kTcProducers) {
-        // ---------------- producers ----------------
-        const uint4 *tabc = tab + (lane & (kTabCopies - 1));
-        uint32_t g = 0;  // chunk counter over all units
-        for (uint32_t k = 0; k < nmine && !failed; ++k) {
-            const int rb = k & 1;
-            if (!wait(&raw_full[rb], (k >> 1) & 1)) break;
-            const TcMeta &m = meta[rb];
-            const int nvalid = m.nvalid, npad = m.npad;
-            const uint8_t *raw = rawb + rb * lay.raw;
-            // B pieces of chunk c for this thread: i = tid + kTcPT * t < npad * 8
-            auto load_b = [&](int c, uint4 (&bv)[kTcBMax]) {
-#pragma unroll
-                for (int t = 0; t < kTcBMax; ++t) {
-                    const int i = tid + kTcPT * t;
-                    const int n = i % npad, j = i / npad;
-                    bv[t] = make_uint4(0u, 0u, 0u, 0u);
-                    if (i < npad * kKG && n < nvalid) {
-                        const uint16_t *src = MODE == 0 ? a.xb16 + (size_t)m.tok[n] * a.H + c * kKC + j * 8
-                                                        : a.hb16 + (size_t)(m.p_lo + n) * a.I + c * kKC + j * 8;
-                        bv[t] = __ldg(reinterpret_cast<const uint4 *>(src));
-                    }
+        // copies still in flight (only after a failure) must land before the CTA exits
+        for (uint32_t j = k >= 2 ? k - 2 : 0; j < k; ++j) mbar_wait_warp(&raw_full[j & 1], (j >> 1) & 1);
+    } else if (warp == kTcBW) {
+        // ---------------- B operand: tensor copies of the unit's activation rows ----------------
+        uint32_t gbs = 0;  // B stages used so far
+        for (uint32_t k = 0;; ++k) {
+            const TcMeta *m = next_meta(k);
+            if (!m) break;
+            const int npad = m->npad, cps = tc_cps(npad, nchunks);
+            const uint32_t p_lo = m->p_lo;
+            for (int bs = 0; bs < nchunks / cps; ++bs) {
+                const int s = gbs % SB;
+                if (gbs >= (uint32_t)SB && !wait_spin(&b_empty[s], ((gbs / SB) - 1) & 1)) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&b_full[s], (uint32_t)(cps * npad * kChunkV * 2));
+                    for (int j = 0; j < cps; ++j)
+                        for (int r = 0; r < npad / 16; ++r)
+                            tma_load_2d(bst + ((size_t)s * kNT + j * npad + 16 * r) * (kChunkV * 2), &args.bmap,
+                                        (bs * cps + j) * kChunkV, (int)p_lo + 16 * r, &b_full[s]);
                 }
-            };
-            uint4 bv[kTcBMax];
-            load_b(0, bv);
-            for (int c = 0; c < nch && !failed; ++c, ++g) {
-                const int s = g % kTcStages;
-                if (g >= (uint32_t)kTcStages && !wait_spin(&st_empty[s], ((g / kTcStages) - 1) & 1)) break;
-                if (aborted()) { failed = true; break; }
-                uint8_t *dA = stg + s * (lay.stA + lay.stB);
-                uint8_t *dB = dA + lay.stA;
-                // B of this chunk (loaded one chunk ahead), then the loads of the next chunk
-#pragma unroll
-                for (int t = 0; t < kTcBMax; ++t) {
-                    const int i = tid + kTcPT * t;
-                    if (i < npad * kKG) {
-                        const int n = i % npad, j = i / npad;
-                        *reinterpret_cast<uint4 *>(dB + ((n >> 3) * kKG + j) * 128 + (n & 7) * 16) = bv[t];
-                    }
-                }
-                if (c + 1 < nch) load_b(c + 1, bv);
-                // A: the 128 x 64 chunk as +-codebook values (exact in 16 bits), no block scale;
-                // all loads of the thread's items first, then the stores
-                uint32_t gs[kTcAItems];
-                int row_[kTcAItems], j_[kTcAItems];
-#pragma unroll
-                for (int t = 0; t < kTcAItems; ++t) {
-                    const int i = tid + kTcPT * t;
-                    const int row = i & 127, j = i >> 7;
-                    row_[t] = row;
-                    j_[t] = j;
-                    gs[t] = 0;
-                    if (i < 128 * kKG) {
-                        int r = row;
-                        const uint8_t *rb_ = raw;
-                        if (MODE == 0 && row >= kGuRows) {  // rows 64..127: the up matrix
-                            r = row - kGuRows;
-                            rb_ = raw + matrix_bytes(kGuRows, a.H);
-                        }
-                        const int G = r * (C / 8) + c * kKG + j;  // flat group index inside the raw rows
-                        gs[t] = *reinterpret_cast<const uint16_t *>(rb_ + (G >> 5) * kBlockBytes + 2 + 2 * (G & 31));
-                    }
-                }
-                uint4 q[kTcAItems];
-#pragma unroll
-                for (int t = 0; t < kTcAItems; ++t) q[t] = tabc[(gs[t] & 0xffu) * kTabCopies];
-#pragma unroll
-                for (int t = 0; t < kTcAItems; ++t) {
-                    if (tid + kTcPT * t < 128 * kKG) {
-                        const uint32_t sgn = (gs[t] >> 8) & 0xffu;
-                        const uint32_t s2 = sgn | ((sgn << 15) & 0x007f0000u);
-                        uint4 v;
-                        v.x = q[t].x ^ ((s2 << 15) & 0x80008000u);
-                        v.y = q[t].y ^ ((s2 << 13) & 0x80008000u);
-                        v.z = q[t].z ^ ((s2 << 11) & 0x80008000u);
-                        v.w = q[t].w ^ ((s2 << 9) & 0x80008000u);
-                        const int row = row_[t];
-                        *reinterpret_cast<uint4 *>(dA + ((row >> 3) * kKG + j_[t]) * 128 + (row & 7) * 16) = v;
-                    }
-                }
-                fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&st_full[s]);
+                ++gbs;
             }
             if (failed) break;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&raw_empty[rb]);
+            if (lane == 0) mbar_arrive(&raw_empty[k & 1]);
         }
-    } else if (warp == kTcMmaWarp) {
-        // ---------------- MMA issuer ----------------
-        uint32_t g = 0;
-        for (uint32_t k = 0; k < nmine && !failed; ++k) {
-            const int ab = k & 1;
-            if (k >= 2 && !wait(&acc_empty[ab], ((k >> 1) - 1) & 1)) break;
-            for (int c = 0; c < nch; ++c, ++g) {
-                const int s = g % kTcStages;
-                if (!wait_spin(&st_full[s], (g / kTcStages) & 1)) break;
-                if (lane == 0) {
-                    tc::fence_after();
-                    const int npad = meta[k & 1].npad;
-                    const uint32_t idesc = tc::instr_desc(TcType<T16>::fmt, 128, npad);
-                    const uint8_t *dA = stg + s * (lay.stA + lay.stB);
-                    const uint32_t aB = tc::s_addr(dA), bB = tc::s_addr(dA + lay.stA);
-                    const int blk = nblk == 1 ? 0 : (c * kKC) / 256;
-                    const bool first = nblk == 1 ? c == 0 : (c * kKC) % 256 == 0;
-                    const uint32_t d = tmem + (uint32_t)(ab * acc_cols + blk * nt);
-#pragma unroll
-                    for (int kk = 0; kk < kKC / 16; ++kk)
-                        tc::mma_f16(d, tc::smem_desc(aB + kk * 256, 128, kKG * 128),
-                                    tc::smem_desc(bB + kk * 256, 128, kKG * 128), idesc, (first && kk == 0) ? 0u : 1u);
-                    tc::commit(&st_empty[s]);
-                    if (c == nch - 1) tc::commit(&acc_full[ab]);
-                }
+        // stages issued but never consumed (only after a failure) must land before the CTA exits
+        for (uint32_t j = gbs >= (uint32_t)SB ? gbs - SB : 0; j < gbs; ++j) mbar_wait_warp(&b_full[j % SB], (j / SB) & 1);
+    } else if (warp < kTcProd) {
+        // ---------------- A producers ----------------
+        // Set J decodes the unit's steps st = J, J + 2, ... (K values [128 st, 128 st + 128))
+        // into stage st % 4, so it fills stages J and J + 2 in turn: one is decoded while the
+        // MMAs read the other.
+        const int q = warp & 3, J = warp >> 2;
+        // gate/up: lanes 0-15 of a quadrant hold gate rows, 16-31 the up rows of the same hidden
+        // units, so that the epilogue pairs them with one shuffle
+        const int rho = MODE == 0 ? (lane < 16 ? 16 * q + lane : kGuUnits + 16 * q + lane - 16) : 32 * q + lane;
+        const uint32_t tabc = smem_addr(tab + (lane & (kTabCopies - 1)));
+        const uint32_t lanebase = tmem + ((uint32_t)(32 * q) << 16);
+        uint32_t used = 0u, par = 0u;  // per stage: filled before; parity of its next fill
+        for (uint32_t k = 0;; ++k) {
+            const TcMeta *m = next_meta(k);
+            if (!m) break;
+            const uint32_t raw = smem_addr(rawb + (k & 1) * lay.rawb);
+            for (int st = J; st < nsteps; st += 2) {
+                const int sg = st % kAStages;
+                // before fill f >= 1 of the stage, the MMAs of fill f - 1 must be done
+                if (((used >> sg) & 1u) && !wait_spin(&a_empty[sg], ((par >> sg) & 1u) ^ 1u)) break;
+                const uint32_t tcol = lanebase + (uint32_t)(sg * kStepV / 2);
+                produce_generic(raw, rho * (C / 8) + st * (kStepV / 8), kStepV / 8, tabc, tcol);
+                tc::st_wait();
+                tc::fence_before();
                 __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[sg]);
+                used |= 1u << sg;
+                par ^= 1u << sg;
             }
+            if (failed) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[k & 1]);
         }
-    } else if (warp >= kTcEpiWarp0) {
-        // ---------------- epilogue ----------------
-        const int quad = warp & 3;                 // TMEM lanes 32 quad .. 32 quad + 31 = A rows
-        const int row = quad * 32 + lane;
-        for (uint32_t k = 0; k < nmine && !failed; ++k) {
-            const int ab = k & 1, rb = k & 1;
-            if (!wait(&acc_full[ab], (k >> 1) & 1)) break;
-            tc::fence_after();
-            const TcMeta &m = meta[rb];
-            const int nvalid = m.nvalid, npad = m.npad, mt = m.mt;
-            const uint8_t *raw = rawb + rb * lay.raw;
-            int r = row;
-            const uint8_t *rr = raw;
-            if (MODE == 0 && row >= kGuRows) {
-                r = row - kGuRows;
-                rr = raw + matrix_bytes(kGuRows, a.H);
-            }
-            float dsc[8];
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                const int G = r * (C / 8) + (nblk == 1 ? 0 : 32 * b);
-                dsc[b] = b < nblk ? fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(rr + (G >> 5) * kBlockBytes))
-                                  : 0.f;
-            }
-            const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(ab * acc_cols);
-            auto scaled16 = [&](int c0, float (&acc)[16]) {
-#pragma unroll
-                for (int q = 0; q < 16; ++q) acc[q] = 0.f;
-                for (int b = 0; b < nblk; ++b) {
-                    uint32_t v[16];
-                    tc::ld16(trow + (uint32_t)(b * nt + c0), v);
-                    tc::ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) acc[q] = fmaf(dsc[b], __uint_as_float(v[q]), acc[q]);
-                }
+    } else if (warp == kTcMmaW) {
+        // ---------------- MMA issuer: lane 0 alone ----------------
+        // Measured on GB300: one thread issues an M = 128, K = 16 MMA at best every ~45 cycles
+        // (the tensor pipe itself needs 64 cycles at N = 128 and 128 at N = 256, whatever the
+        // source of A), and every instruction the issuing thread adds around the MMAs slows the
+        // issue further.  At the ~10 pairs per expert of a 512-token chunk the grouped GEMM is
+        // bound by this issue rate, so the path is kept short: descriptors built once per B
+        // chunk and advanced by constants, a constant accumulate predicate after the unit's first
+        // K step, no warp-wide synchronisation.
+        if (lane == 0) {
+            auto spin1 = [&](uint64_t *bar, uint32_t parity) {
+                for (uint32_t i = 0; i < kSpinPolls; ++i)
+                    if (mbar_test_wait(bar, parity)) return true;
+                atomicExch(abort_s, 1);
+                failed = true;
+                return false;
             };
-            if (MODE == 0) {
-                if (row >= kGuRows) {  // up rows: park u once the gate rows have used the last one
-                    if (k >= 1 && !wait(ex_empty, (k - 1) & 1)) break;
-                    for (int c0 = 0; c0 < npad; c0 += 16) {
-                        float acc[16];
-                        scaled16(c0, acc);
+            const uint32_t bst_s = tc::s_addr(bst);
+            uint32_t gbs = 0, par = 0u;  // B stages consumed; per A stage, parity of its next fill
+            for (uint32_t k = 0; !aborted(); ++k) {
+                if (!spin1(&raw_full[k & 1], (k >> 1) & 1)) break;
+                const TcMeta *m = &meta[k & 1];
+                if (m->end) break;
+                const int npad = m->npad, cps = tc_cps(npad, nchunks);
+                const uint32_t idesc = tc::instr_desc(0u, kTcRows, npad);
+                const uint32_t cstride = (uint32_t)(npad * kChunkV * 2);  // bytes between the chunks of a stage
+                mbar_arrive(&raw_empty[k & 1]);  // the metadata is no longer needed here
+                const int ab = k & 1;
+                if (k >= 2 && !spin1(&acc_empty[ab], ((k >> 1) - 1) & 1)) break;
+                const uint32_t d = tmem + kAccCol0 + (uint32_t)(ab * kNT);
+                int s = 0, j = 0;
+                uint32_t bc = 0;
+                for (int st = 0; st < nsteps; ++st) {
+                    const int sg = st % kAStages;
+                    if (!spin1(&a_full[sg], (par >> sg) & 1u)) break;
+                    par ^= 1u << sg;
+                    tc::fence_after();
+                    const uint32_t a0 = tmem + (uint32_t)(sg * kStepV / 2);
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) u_s[r * nt + c0 + q] = acc[q];
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(ex_full);
-                } else {               // gate rows: h = silu(g) * u
-                    if (!wait(ex_full, k & 1)) break;
-                    uint16_t *hb = a.hb16 + (size_t)m.p_lo * a.I + (size_t)mt * kGuRows + r;
-                    for (int c0 = 0; c0 < npad; c0 += 16) {
-                        float acc[16];
-                        scaled16(c0, acc);
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            const int n = c0 + q;
-                            if (n < nvalid) hb[(size_t)n * a.I] = (uint16_t)TcType<T16>::bits(silu(acc[q]) * u_s[r * nt + n]);
+                    for (int c = 0; c < kStepV / kChunkV; ++c) {
+                        if (j == 0) {
+                            s = gbs % SB;
+                            if (!spin1(&b_full[s], (gbs / SB) & 1)) break;
+                            tc::fence_after();
+                            bc = bst_s + (uint32_t)(s * kNT * kChunkV * 2);
+                        }
+                        const uint64_t bd = tc::smem_desc_sw128(bc, 1024);
+                        const uint32_t ac = a0 + (uint32_t)(c * kChunkV / 2);
+                        if (st == 0 && c == 0)
+                            tc::mma_f16_ts(d, ac, bd, idesc, 0u);
+                        else
+                            tc::mma_f16_ts_acc(d, ac, bd, idesc);
+                        tc::mma_f16_ts_acc(d, ac + 8, bd + 2, idesc);   // +32 bytes of B: start address field + 2
+                        tc::mma_f16_ts_acc(d, ac + 16, bd + 4, idesc);
+                        tc::mma_f16_ts_acc(d, ac + 24, bd + 6, idesc);
+                        bc += cstride;
+                        if (++j == cps) {
+                            tc::commit(&b_empty[s]);
+                            ++gbs;
+                            j = 0;
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(ex_empty);
+                    if (failed) break;
+                    tc::commit(&a_empty[sg]);
                 }
-            } else {
-                const int orow = mt * kDnRowsTc + row;  // output row of H
-                for (int c0 = 0; c0 < npad; c0 += 16) {
-                    float acc[16];
-                    scaled16(c0, acc);
+                if (failed) break;
+                tc::commit(&acc_full[ab]);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kTcEpi0) {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + kAccCol0;
+        for (uint32_t k = 0;; ++k) {
+            const TcMeta *m = next_meta(k);
+            if (!m) break;
+            const int ab = k & 1;
+            if (!wait_spin(&acc_full[ab], (k >> 1) & 1)) break;
+            tc::fence_after();
+            const int nvalid = m->nvalid, npad = m->npad, mt = m->mt;
+            const uint32_t p_lo = m->p_lo;
+            for (int c0 = 0; c0 < npad; c0 += 16) {
+                uint32_t v[16];
+                tc::ld16(trow + (uint32_t)(ab * kNT + c0), v);
+                tc::ld_wait();
+                if (MODE == 0) {
+                    // lane < 16: gate row of hidden unit hu, lane + 16: its up row.  The gate lane
+                    // takes columns c0..c0+7, the up lane c0+8..c0+15.
+                    const bool gate = lane < 16;
+                    const int hu = mt * kGuUnits + 16 * q + (lane & 15);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int n = c0 + q;
-                        if (n < nvalid) a.outbuf[((size_t)m.tok[n] * a.K + m.k[n]) * a.H + orow] = acc[q];
+                    for (int j = 0; j < 8; ++j) {
+                        const float mine = __uint_as_float(gate ? v[j] : v[8 + j]);
+                        const float send = __uint_as_float(gate ? v[8 + j] : v[j]);
+                        const float other = __shfl_xor_sync(kFull, send, 16);
+                        const float g = gate ? mine : other, u = gate ? other : mine;
+                        const int n = c0 + (gate ? j : 8 + j);
+                        if (n < nvalid)
+                            a.hb16[(size_t)(p_lo + n) * a.I + hu] = __half_as_ushort(__float2half_rn(silu(g) * u));
+                    }
+                } else {
+                    const int orow = mt * kTcRows + 32 * q + lane;  // output row of H
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = c0 + j;
+                        if (n < nvalid)
+                            a.outbuf[((size_t)m->tok[n] * a.K + m->kk[n]) * a.H + orow] = __uint_as_float(v[j]);
                     }
                 }
             }
@@ -515,60 +537,75 @@ __global__ void __launch_bounds__(kTcThreads2, 1) tc_gemm_kernel(PrefillArgs a, 
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&acc_empty[ab]);
-                mbar_arrive(&raw_empty[rb]);
+                mbar_arrive(&raw_empty[k & 1]);
             }
         }
     }
     if (failed && lane == 0) dev_error(a.ctrl, RL_DEVERR_WAIT_TIMEOUT);
     // drain every tcgen05 operation this CTA issued, then release tensor memory
     __syncthreads();
-    if (tid == kTcMmaWarp * 32) {
+    if (tid == kTcMmaW * 32) {
         tc::commit(fin_bar);
         if (!mbar_wait(fin_bar, 0)) dev_error(a.ctrl, RL_DEVERR_WAIT_TIMEOUT);  // the drain did not finish
     }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    if (warp == 0) tc::tmem_dealloc(tmem, 512);
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T16>
-static rl_status run_tc(const PrefillArgs &a0, cudaStream_t s) {
-    PrefillArgs a = a0;
+// the B operand [rows][C] f16 as a tensor map: boxes of 64 values x 16 rows, 128-byte swizzle
+static rl_status b_tensor_map(CUtensorMap *map, const uint16_t *base, int rows, int C) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+    if (!enc) return fail(RL_ERR_CUDA, "moe_prefill_chunk: cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t gdim[2] = {(cuuint64_t)C, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kChunkV, 16u};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult cr = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(base), gdim, gstride, box,
+                            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(RL_ERR_CUDA, "moe_prefill_chunk: tensor map rejected (error %d)", (int)cr);
+    return RL_OK;
+}
+
+template <int MODE>
+static rl_status launch_tc(const TcArgs &args, int grid, cudaStream_t s) {
+    const TcLayout lay(MODE, args.a.H, args.a.I);
+    auto kern = tc_gemm_kernel<MODE>;
+    rl_status st = allow_smem((const void *)kern, lay.total);
+    if (st != RL_OK) return st;
+    kern<<<grid, kTcThreads, lay.total, s>>>(args);
+    return check_launch(MODE == 0 ? "moe_prefill_chunk gate/up" : "moe_prefill_chunk down");
+}
+
+static rl_status run_tc(const PrefillArgs &a, cudaStream_t s) {
     const int P = a.P, E = a.E;
-    const int gu_tiles = a.I / kGuRows, dn_tiles = a.H / kDnRowsTc;
+    const int gu_tiles = a.I / kGuUnits, dn_tiles = a.H / kTcRows;
     TcUnits U;
     uint8_t *ub = reinterpret_cast<uint8_t *>(a.units);
     U.counts = reinterpret_cast<uint32_t *>(ub);
-    const int nt_gu = tc_nt2(a.H), nt_dn = tc_nt2(a.I);
-    U.max_gu = tc_max_units(P, E, nt_gu, gu_tiles);
-    U.max_dn = tc_max_units(P, E, nt_dn, dn_tiles);
+    const size_t nb = tc_max_blocks(P, E);
     U.gu = reinterpret_cast<uint32_t *>(ub + 256);
-    U.dn = U.gu + U.max_gu;
-    const size_t n = (size_t)a.T * a.H;
-    tc_convert_kernel<T16><<<(int)std::min<size_t>((n + 255) / 256, 4096), 256, 0, s>>>(a.xn, a.xb16, n, a.ctrl,
-                                                                                       a.layer);
-    tc_units_kernel<<<1, 512, 0, s>>>(a.offs, E, nt_gu, gu_tiles, nt_dn, dn_tiles, U.counts, U.gu, U.dn, a.ctrl,
-                                      a.layer);
+    U.dn = U.gu + nb * gu_tiles;
+    tc_gather_kernel<<<(P + 7) / 8, 256, 0, s>>>(a.xn, a.pair_tok, a.xb16, P, a.H, a.ctrl, a.layer);
+    tc_units_kernel<<<1, 512, 0, s>>>(a.offs, E, gu_tiles, dn_tiles, U.counts, U.gu, U.dn, a.ctrl, a.layer);
     rl_status st = check_launch("moe_prefill_chunk setup");
     if (st != RL_OK) return st;
     const int sms = sm_count();
-    {
-        const TcLayout lay(0, a.H, a.I);
-        st = allow_smem((const void *)tc_gemm_kernel<T16, 0>, lay.total);
-        if (st != RL_OK) return st;
-        tc_gemm_kernel<T16, 0><<<(int)std::min<size_t>(sms, U.max_gu), kTcThreads2, lay.total, s>>>(a, U);
-        st = check_launch("moe_prefill_chunk gate/up");
-        if (st != RL_OK) return st;
-    }
-    {
-        const TcLayout lay(1, a.H, a.I);
-        st = allow_smem((const void *)tc_gemm_kernel<T16, 1>, lay.total);
-        if (st != RL_OK) return st;
-        tc_gemm_kernel<T16, 1><<<(int)std::min<size_t>(sms, U.max_dn), kTcThreads2, lay.total, s>>>(a, U);
-        st = check_launch("moe_prefill_chunk down");
-        if (st != RL_OK) return st;
-    }
+    TcArgs args;
+    args.a = a;
+    args.U = U;
+    const int P16 = P > 16 ? P : 16;  // rows of the operand buffers (the workspace holds at least 16)
+    st = b_tensor_map(&args.bmap, a.xb16, P16, a.H);
+    if (st != RL_OK) return st;
+    const int g_gu = (int)std::min<size_t>(sms, nb * gu_tiles), g_dn = (int)std::min<size_t>(sms, nb * dn_tiles);
+    st = launch_tc<0>(args, g_gu, s);
+    if (st != RL_OK) return st;
+    st = b_tensor_map(&args.bmap, a.hb16, P16, a.I);
+    if (st != RL_OK) return st;
+    st = launch_tc<1>(args, g_dn, s);
+    if (st != RL_OK) return st;
     return launch_ordered_sum(a, s);
 }
 
@@ -585,5 +622,5 @@ extern "C" rl_status moe_prefill_chunk(const rl_moe_shape *shp, int32_t layer, i
     rl_status st = prefill_check(shp, layer, T, xn, offs, pair_tok, pair_k, slots, weights, codebook, y, accumulate,
                                  ctrl, ws, ws_bytes, "moe_prefill_chunk", &a);
     if (st != RL_OK || T == 0) return st;
-    return run_tc<__nv_bfloat16>(a, as_stream(stream));
+    return run_tc(a, as_stream(stream));
 }

@@ -1,6 +1,8 @@
 // rl_common.cuh - shared device helpers and host-side argument checks of librlmoe.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -29,6 +31,20 @@ rl_status check_shape(const rl_moe_shape *shp);
 __host__ __device__ inline size_t matrix_bytes(int rows, int cols) { return (size_t)rows * cols / kBlockValues * kBlockBytes; }
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+// cuTensorMapEncodeTiled, from the driver through the runtime (no link to the driver library);
+// NULL when the driver does not provide it
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
 // opt a kernel into more than 48 KB of dynamic shared memory (idempotent)
 rl_status allow_smem(const void *kernel, size_t bytes);
 // streaming multiprocessors of the current device (cached)
@@ -100,6 +116,17 @@ __device__ __forceinline__ float fp16_bits_to_float(uint32_t bits) {
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// explicit shared-memory loads at a shared-window address (never resolved as generic loads)
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
 }
 
 // ---- mbarrier + bulk async copy (global -> this CTA's shared memory) ----------------------
@@ -180,6 +207,16 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_addr(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+// 2-D tensor copy of one box of `map` at element coordinates (x, y) into shared memory;
+// completion is signalled as transaction bytes on `bar`.  x times the element size must be a
+// multiple of 16 bytes; rows and columns outside the tensor read as zeros.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
 }
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src_gmem, uint32_t bytes) {

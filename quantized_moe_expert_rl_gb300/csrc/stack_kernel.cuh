@@ -43,9 +43,6 @@
 // RL_DEVERR_WAIT_TIMEOUT, waits (bounded) for its own copies in flight and returns; the other
 // CTAs then time out at their next barrier.
 #pragma once
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "decode_rows.cuh"
 #include "select.cuh"
 
@@ -145,13 +142,6 @@ struct StackArgs {
     int layer0, nl, H, E, K, I, pregate, n_layers;
 };
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-        : "memory");
-}
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
     unsigned long long v;
@@ -722,19 +712,6 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     cta_sync();
 }
 
-// cuTensorMapEncodeTiled, from the driver through the runtime (no link to the driver library)
-static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
 
 template <int NV, int GPL, int SPLIT, int DGPL, int LPR, bool FILL>
 static rl_status launch_stack(StackArgs a, cudaStream_t s) {

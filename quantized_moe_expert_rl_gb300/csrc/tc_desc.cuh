@@ -9,6 +9,13 @@
 //   8 rows x 16 bytes (8 rows x 8 16-bit elements, rows contiguous): LBO is the byte distance
 //   between the two K-adjacent core matrices of one K=16 slice, SBO the byte distance between
 //   M/N-adjacent groups of 8 rows.
+//   With the 128-byte swizzle (layout 2) a K-major operand is stored as rows of 128 bytes (64
+//   16-bit values), 8-row atoms of 1024 bytes whose 16-byte chunks are XOR-permuted by the row
+//   index (the pattern a TMA copy with CU_TENSOR_MAP_SWIZZLE_128B writes); SBO is the distance
+//   between 8-row atoms and the start address moves by 32 bytes per K = 16 step.
+//   A operand in tensor memory (tcgen05.mma [d], [a], b_desc, ...): lane m holds row m, and
+//   32-bit column c holds the 16-bit values k = 2c (low half) and 2c + 1 (high half); one
+//   K = 16 step reads 8 columns.
 //   instruction descriptor for kind::f16 (32 bit)
 //     [4,6) D format: 1 = f32   [7,10) A format, [10,13) B format: 0 = f16, 1 = bf16
 //     [15] A major, [16] B major: 0 = K-major   [17,23) N >> 3   [24,29) M >> 4
@@ -23,6 +30,12 @@ namespace tc {
 __host__ __device__ constexpr uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// K-major operand with the 128-byte swizzle, 8-row atoms `sbo` bytes apart (1024 when packed)
+__host__ __device__ constexpr uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46) | (2ull << 61);
 }
 
 // ab_fmt: 0 = f16, 1 = bf16 (A and B always share one type)
@@ -56,6 +69,23 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, one elected thread; A from tensor memory at a_tmem
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// the same, always accumulating (D += A B^T): no run-time predicate on the issue path
+__device__ __forceinline__ void mma_f16_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, 1, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc)
+        : "memory");
+}
 // arrive once on the mbarrier when every tcgen05 operation issued so far by this thread is done
 __device__ __forceinline__ void commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s_addr(bar))
@@ -70,6 +100,19 @@ __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 __device__ __forceinline__ void ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 32 consecutive 32-bit columns from registers: thread i of the warp writes lane
+// (base lane + i); completion is awaited with st_wait()
+__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Ampere-style asynchronous 16-byte global -> shared copy (L2 only), tracked by groups
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {

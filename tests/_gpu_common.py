@@ -10,7 +10,7 @@ import oracle
 import synth
 
 REL_F32 = 1e-5        # relative L2 bound of the f32 CUDA-core paths
-REL_BF16 = 5e-3       # relative L2 bound of the bf16 tensor-core path
+REL_TC = 5e-3         # relative L2 bound of the tensor-core path (16-bit operands, f32 accumulate)
 W_ABS = 1e-6          # renormalised weights, absolute
 # Router logits against the oracle's f64 logits, relative to the row's largest |logit|.
 # rl_route forms each logit as one f32 dot product (at most a few hundred sequential terms

@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 import oracle  # noqa: E402
 import synth  # noqa: E402
-from tests._gpu_common import LOGIT_FIXED, REL_BF16, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
+from tests._gpu_common import LOGIT_FIXED, REL_TC, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
 
 TINY = synth.WORKLOADS["tiny"]
 DEGENERATE = {
@@ -81,7 +81,7 @@ def test_prefill_ragged_chunks(T, path):
     o = OracleSide(m)
     x = torch.from_numpy(synth.tokens(w)).cuda()
     y, y_o, _ = _prefill(engine, w, m, o, x, path)
-    assert rel_l2(y, y_o) <= (REL_F32 if path == "f32" else REL_BF16)
+    assert rel_l2(y, y_o) <= (REL_F32 if path == "f32" else REL_TC)
 
 
 @pytest.mark.parametrize("name", sorted(DEGENERATE))
@@ -107,7 +107,7 @@ def test_degenerate_routing_decode_and_prefill(name):
         assert rel_l2(y[t].cpu().numpy(), o.experts(xo, r.ids, r.weights, r.slots)[0]) <= REL_F32
     assert b.ctrl.tolist() == [0x7FFFFFFF, 0]
     # the same tokens as one chunk, on both grouped paths
-    for path, tol in (("f32", REL_F32), ("tc", REL_BF16)):
+    for path, tol in (("f32", REL_F32), ("tc", REL_TC)):
         yp, y_o, r = _prefill(engine, w, m, o, x, path)
         assert rel_l2(yp, y_o) <= tol, (path, rel_l2(yp, y_o))
 

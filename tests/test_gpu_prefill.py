@@ -10,9 +10,9 @@ pytestmark = pytest.mark.gpu
 
 import oracle  # noqa: E402
 import synth  # noqa: E402
-from tests._gpu_common import REL_BF16, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
+from tests._gpu_common import REL_TC, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
 
-PATHS = [("f32", REL_F32), ("tc", REL_BF16)]
+PATHS = [("f32", REL_F32), ("tc", REL_TC)]
 
 
 def _engine():
@@ -60,7 +60,7 @@ def test_prefill_chunk(chunk_model, path, tol):
 
 
 def test_prefill_paths_agree(chunk_model):
-    """The two grouped paths on the same routing: bf16 tensor-core result within the bf16
+    """The two grouped paths on the same routing: tensor-core result within the tensor-core
     bound of the f32 CUDA-core result over every token."""
     engine = _engine()
     w, m, _ = chunk_model
@@ -73,7 +73,7 @@ def test_prefill_paths_agree(chunk_model):
         engine.enqueue_prefill_experts(m, b, 0, x, y, stacked=False, path=path)
         torch.cuda.synchronize()
         ys[path] = y.double().cpu().numpy()
-    assert rel_l2(ys["tc"], ys["f32"]) <= REL_BF16
+    assert rel_l2(ys["tc"], ys["f32"]) <= REL_TC
 
 
 @pytest.fixture(scope="module")

@@ -8,7 +8,7 @@ pytestmark = pytest.mark.gpu
 
 import oracle  # noqa: E402
 import synth  # noqa: E402
-from tests._gpu_common import REL_BF16, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
+from tests._gpu_common import REL_TC, REL_F32, OracleSide, check_route, rel_l2, u64  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -65,5 +65,5 @@ def test_prefill_chunk(tiny, path):
     assert np.array_equal(b.pair_tok[:P].cpu().numpy().astype(np.uint32), ptok)
     assert np.array_equal(b.pair_k[:P].cpu().numpy(), pk)
     y_o = o.experts(xo, r.ids, r.weights, r.slots)
-    tol = REL_F32 if path == "f32" else REL_BF16
+    tol = REL_F32 if path == "f32" else REL_TC
     assert rel_l2(y.cpu().numpy(), y_o) <= tol

@@ -24,6 +24,7 @@ def encoded(tmp_path_factory):
                    ' printf("%x\\n", rl::tc::instr_desc(1u, 128, 16));\n'
                    ' printf("%x\\n", rl::tc::instr_desc(0u, 128, 128));\n'
                    ' printf("%x\\n", rl::tc::instr_desc(1u, 64, 256));\n'
+                   ' printf("%llx\\n", (unsigned long long)rl::tc::smem_desc_sw128(0x21000u, 1024u));\n'
                    " return 0;}\n")
     exe = d / "enc"
     subprocess.run([nvcc, "-std=c++17", "-I", CSRC, "-o", str(exe), str(src)], check=True)
@@ -45,3 +46,9 @@ def test_instruction_descriptor(encoded):
     assert int(encoded[3], 16) == 0x08200010
     # M = 64 -> 4 << 24; N = 256 -> 32 << 17
     assert int(encoded[4], 16) == (1 << 4) | (1 << 7) | (1 << 10) | (32 << 17) | (4 << 24)
+
+
+def test_swizzled_descriptor(encoded):
+    # 128-byte swizzle, K-major: start 0x21000 >> 4 = 0x2100; LBO field 1 (unused with this
+    # layout); SBO 1024 >> 4 = 64 at bit 32; version 1 at bit 46; layout 2 in bits 61-63
+    assert int(encoded[5], 16) == 0x2100 | (1 << 16) | (64 << 32) | (1 << 46) | (2 << 61)

@@ -201,3 +201,98 @@ __device__ __forceinline__ void cta_topk_thr(uint32_t key, const uint64_t *__res
 }
 
 }  // namespace rl
+
+namespace rl {
+
+// Top-k of up to 512 keys by ONE warp, in a few dependent steps, so that every warp of a CTA
+// can select on its own with no CTA barrier after the keys are written.  keys_t holds the key
+// of expert e at [(e % 16) * 32 + e / 16] (0 for absent experts and for e >= E), so lane L
+// reads the keys of experts 16 L .. 16 L + 15 with conflict-free loads and lower lanes hold
+// lower indices.  Let m_L be lane L's largest key and T the K-th largest of the 32 m_L: the K
+// lanes holding the K largest give K keys >= T, so every key of the top-K is >= T.  The keys
+// >= T (a few tens at most, usually) are gathered into the warp's scratch and each is ranked
+// exactly against the others in the order (logit descending, index ascending); with more than
+// 32 candidates (heavy ties) K rounds of warp arg-max take over.  The selection equals
+// warp_topk's.  Scratch: ck[32], ci[32], sel[kMaxK] of this warp.  Lane r < K ends with the
+// r-th selection; the warp is converged on return.
+__device__ __forceinline__ void warp_topk_thr(const uint32_t *keys_t, int E, int K, uint32_t *ck, int *ci, int *sel,
+                                              int &my_id, float &my_val) {
+    const int lane = threadIdx.x & 31;
+    uint32_t k[16];
+    uint32_t m = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        k[j] = keys_t[j * 32 + lane];
+        m = k[j] > m ? k[j] : m;
+    }
+    int rank = 0;  // rank of m among the lane maxima (ties by lane)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t mj = __shfl_sync(kFull, m, j);
+        rank += (mj > m || (mj == m && j < lane)) ? 1 : 0;
+    }
+    const uint32_t T = __shfl_sync(kFull, m, __ffs(__ballot_sync(kFull, rank == K - 1)) - 1);
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) cnt += (16 * lane + j < E && k[j] >= T) ? 1 : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += u;
+    }
+    const int n = __shfl_sync(kFull, incl, 31);
+    my_id = 0;
+    my_val = 0.f;
+    if (n <= 32) {
+        int at = incl - cnt;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (16 * lane + j < E && k[j] >= T) {
+                ck[at] = k[j];
+                ci[at] = 16 * lane + j;
+                ++at;
+            }
+        __syncwarp();
+        // lane c holds candidate c and ranks it against the others through shuffles
+        const uint32_t kc = lane < n ? ck[lane] : 0u;
+        const int ic = lane < n ? ci[lane] : 0x7fffffff;
+        int r = 0;
+#pragma unroll
+        for (int d = 0; d < 32; ++d) {
+            const uint32_t kd = __shfl_sync(kFull, kc, d);
+            const int id = __shfl_sync(kFull, ic, d);
+            r += (d < n && precedes(kd, id, kc, ic)) ? 1 : 0;
+        }
+        if (lane < n && r < K) sel[r] = lane;
+        __syncwarp();
+        if (lane < K) {
+            const int c = sel[lane];
+            my_id = ci[c];
+            my_val = key_value(ck[c]);
+        }
+        __syncwarp();
+    } else {
+        warp_topk_by<16>([&](int e) { return e < E ? keys_t[(e & 15) * 32 + (e >> 4)] : 0u; }, K, my_id, my_val);
+    }
+}
+
+// RMSNorm scale of x (H = NV * 128 values) read through L2 (x written by other CTAs of the
+// same launch), every load issued before the arithmetic: the arithmetic and order of
+// rms_scale_warp exactly, so every path normalises identically.
+template <int NV>
+__device__ __forceinline__ float rms_scale_warp_cg(const float *x, float eps) {
+    const int lane = threadIdx.x & 31;
+    float4 v[NV];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) v[m] = __ldcg(reinterpret_cast<const float4 *>(x + lane * 4 + 128 * m));
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+        a0 = fmaf(v[m].x, v[m].x, a0); a1 = fmaf(v[m].y, v[m].y, a1); a2 = fmaf(v[m].z, v[m].z, a2); a3 = fmaf(v[m].w, v[m].w, a3);
+    }
+    float ss = warp_sum((a0 + a1) + (a2 + a3));
+    return 1.0f / sqrtf(ss / (float)(NV * 128) + eps);
+}
+
+}  // namespace rl

@@ -51,14 +51,18 @@ namespace rl {
 constexpr int kStThreads = 512;
 constexpr int kStWarps = kStThreads / 32;
 constexpr int kStGuChunks = 2;
-constexpr int kStBars = 2 + 2 * kStGuChunks;  // [0] down rows, [1] router columns, [2..] gate/up chunks
+constexpr int kStBars = 3 + 2 * kStGuChunks;  // [0] down rows, [1] router columns, [2..] gate/up chunks, [last] table row
 constexpr uint32_t kSpinCap = 1u << 22;       // global-memory polls (~1 us each): seconds
 constexpr int kStSelWarps = 16;               // selection warps: E <= 32 * 16, one expert per thread
 constexpr int kStHdr = 1024;                  // barriers, scalars, CTA constants, outputs of the selection
 constexpr int kStPredMax = 32;                // experts prefetched on the pre-gated prediction
 constexpr int kStCand = 16;                   // single-warp selection: candidates per lane (E <= 512)
-// selection scratch: keys, ids and table entries of up to 512 candidates, warp maxima, result, count
-constexpr int kStSelBytes = 512 * (4 + 4 + 8) + 64 + 64 + 16;
+// selection scratch: the 512 keys (transposed for warp_topk_thr), per warp 32 candidate keys,
+// 32 candidate ids and kMaxK results, then the layer's residency row (u64, copied ahead)
+constexpr int kStSelWarpBytes = (32 + 32 + kMaxK) * 4;
+constexpr int kStSelTab = 512 * 4 + kStWarps * kStSelWarpBytes;
+constexpr int kStSelBytes = kStSelTab + 512 * 8;
+static_assert(kStSelTab % 16 == 0, "the residency row copy needs a 16-byte aligned destination");
 // The warp that issues every bulk copy.  A memory fence waits for the bulk copies its own
 // thread has in flight, so the thread that runs the grid barrier (thread 0) never issues one.
 constexpr int kStProducer = kStWarps - 1;
@@ -203,11 +207,11 @@ template <int NV, int GPL, int SPLIT, int DGPL, int LPR, bool FILL>
 __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_constant__ StackArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *bar_dn = bars, *bar_rc = bars + 1, *bar_gu = bars + 2;
+    uint64_t *bar_dn = bars, *bar_rc = bars + 1, *bar_gu = bars + 2, *bar_tab = bars + 2 + 2 * kStGuChunks;
     float *scale_s = reinterpret_cast<float *>(smem + 64);
     int *stop_s = reinterpret_cast<int *>(smem + 68);
     int *ok_s = reinterpret_cast<int *>(smem + 72);
-    int *iss_s = reinterpret_cast<int *>(smem + 76);  // copies issued at the end of C: bit 0 down rows, bit 1 router columns
+    int *iss_s = reinterpret_cast<int *>(smem + 76);  // copies issued at the end of C: bit 0 down rows, bit 1 router columns, bit 2 residency row
     StCta &C = *reinterpret_cast<StCta *>(smem + 128);
     uint64_t *slots_s = reinterpret_cast<uint64_t *>(smem + 256);
     float *w_s = reinterpret_cast<float *>(smem + 384);   // [K] weights
@@ -266,6 +270,42 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 tma_load_2d(smem + C.o_rc + (size_t)q * C.rcb + (size_t)k * C.rbs, &a.wmap,
                             C.q0, (a.layer0 + i + q) * E + k * rows, bar_rc);
     };
+    // The residency row of layer index i into shared memory (read by every warp's selection);
+    // completion on bar_tab, whose n-th phase is layer index n.  Rows are 16-byte pieces when E
+    // is even; otherwise the selection reads the table through L2.
+    const bool tab_smem = (E & 1) == 0 && (reinterpret_cast<uintptr_t>(a.table) & 15) == 0;
+    const uint64_t *table_s = reinterpret_cast<const uint64_t *>(smem + C.o_sel + kStSelTab);
+    auto issue_tab = [&](int i) {
+        mbar_arrive_expect_tx(bar_tab, (uint32_t)(E * sizeof(uint64_t)));
+        bulk_g2s(smem + C.o_sel + kStSelTab, a.table + (size_t)(a.layer0 + i) * E, (uint32_t)(E * sizeof(uint64_t)), bar_tab);
+    };
+    // The gate/up copies of the CTA's row pairs (the producer warp, whole warp): lane i <
+    // 2 * kStGuChunks issues chunk (segment i / kStGuChunks, part i % kStGuChunks), its gate
+    // rows and its up rows, completion on bar_gu[i]; sa, sb: the records of experts ka and kb.
+    // Only the copies C needs first are issued here; the down rows and the next layer's router
+    // columns wait until the end of C.
+    auto issue_gu = [&](uint64_t sa, uint64_t sb) {
+        fence_proxy_async_smem();
+        if (FILL) asm volatile("fence.proxy.async.global;" ::: "memory");  // records filled by the device
+        const int I = a.I, rowb = C.rowb;
+        const size_t matb = matrix_bytes(I, H);
+        if (lane < 2 * kStGuChunks && C.p1 > C.p0) {
+            const int seg = lane / kStGuChunks, ch = lane % kStGuChunks;
+            const int n = seg == 0 ? C.n0 : C.n1;
+            const int r0 = gu_cut(C, U, seg, ch), r1 = gu_cut(C, U, seg, ch + 1);
+            if (r1 > r0) {
+                const uint8_t *base = reinterpret_cast<const uint8_t *>(seg == 0 ? sa : sb);
+                const int ia = seg == 0 ? C.p0 - C.ka * I : 0;
+                const uint32_t bytes = (uint32_t)((r1 - r0) * rowb);
+                uint8_t *gdst = smem + C.o_gu + (seg == 0 ? 0 : 2 * (size_t)C.n0 * rowb) + (size_t)r0 * rowb;
+                mbar_arrive_expect_tx(&bar_gu[lane], 2 * bytes);
+                bulk_g2s(gdst, base + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
+                bulk_g2s(gdst + (size_t)n * rowb, base + matb + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
+            }
+        }
+        if (lane == 0) *iss_s = 0;
+        __syncwarp();
+    };
     // This CTA's partial router dots of layer index i on its slice of x_{layer0 + i} (in the
     // shared xq slice), added into acc[i & 1]; pre-gating, the next layer's dots into
     // acc_pg[i & 1].  The columns have landed (bar_rc, waited by the caller).  Each dot runs
@@ -304,11 +344,16 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     bool ex_issued = false;         // this layer's expert copies are in flight
     int rc_pend = -1;               // layer index whose router columns are in flight (-1: none)
     bool failed = false;
+    int tab_pend = -1;              // layer index whose residency row copy is in flight (-1: none)
     // ---- prologue: the accumulators start from zero (CTA 0 clears them; a grid barrier orders
     // the clear before any CTA's sums), then every CTA adds the dots of its slice of x_{layer0}
     if (C.nq > 0) {
         if (threadIdx.x == kColThread) issue_cols(0);
         rc_pend = 0;
+    }
+    if (tab_smem) {
+        if (threadIdx.x == kColThread) issue_tab(0);
+        tab_pend = 0;
     }
     if (blockIdx.x == 0)
         for (int j = threadIdx.x; j < 2 * E; j += kStThreads) {
@@ -331,35 +376,31 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         const int l = a.layer0 + i;
         const bool last = i + 1 == a.nl;
         ex_issued = false;
-        // ---------------- B: x_l, its scale, the logits, the selection (the same in every CTA) ----------------
+        // ---------------- B: the logits, the selection (every warp on its own), x_l ----------------
+        // All threads read their logit accumulator while warp 0 forms the RMSNorm scale of x_l
+        // straight from L2; one CTA barrier, then the keys; one more, then every warp selects
+        // the top-k by itself, so the producer warp issues the expert copies from its own
+        // selection while the others stage x_l for the gate/up lanes.
         const long long accv = me < E ? __ldcg(a.acc + (size_t)(i & 1) * E + me) : 0ll;
-        {
-            float *x_s = reinterpret_cast<float *>(smem + C.o_x);
-            float4 *xt_s = reinterpret_cast<float4 *>(smem + C.o_xt);
-            // x_s in order; xt_s lane-transposed for the gate/up lanes: float4 q of the slice of
-            // lane L of row half h (columns h H/SPLIT + L 8 GPL ...) sits at [h][q][L ^ q] (the
-            // xor spreads the staging writes of consecutive q over the banks)
-            for (int j = threadIdx.x; j < H / 4; j += kStThreads) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.x) + j);
-                reinterpret_cast<float4 *>(x_s)[j] = v;
-                const int hf = H / 4 / SPLIT, h = j / hf, r = j % hf, L = r / (2 * GPL), q = r % (2 * GPL);
-                xt_s[(h * 2 * GPL + q) * 32 + (L ^ q)] = v;
-            }
-            cta_sync();
-            if (warp == 0) {
-                const float r = a.eps >= 0.f ? rms_scale_warp(x_s, H, a.eps) : 1.f;
-                if (lane == 0) *scale_s = r;
-            }
-            if (a.x_hist && blockIdx.x == 0)
-                for (int j = threadIdx.x; j < H; j += kStThreads) a.x_hist[(size_t)l * H + j] = x_s[j];
-            // acc_pg[(i + 1) & 1] was last read in D of the previous layer; it takes this
-            // layer's pre-gate sums next
-            if (pregate && i > 0 && blockIdx.x == 0)
-                for (int j = threadIdx.x; j < E; j += kStThreads) __stcg(a.acc_pg + (size_t)((i + 1) & 1) * E + j, 0ll);
-            cta_sync();
+        // this thread's share of x_l, loaded now and staged after the selection
+        constexpr int kXv = (H / 4 + kStThreads - 1) / kStThreads;
+        float4 xv_r[kXv];
+#pragma unroll
+        for (int u = 0; u < kXv; ++u) {
+            const int j = threadIdx.x + u * kStThreads;
+            xv_r[u] = j < H / 4 ? __ldcg(reinterpret_cast<const float4 *>(a.x) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        {
-            const int K = a.K;
+        if (warp == 0) {
+            const float r = a.eps >= 0.f ? rms_scale_warp_cg<NV>(a.x, a.eps) : 1.f;
+            if (lane == 0) *scale_s = r;
+        }
+        // acc_pg[(i + 1) & 1] was last read in D of the previous layer; it takes this
+        // layer's pre-gate sums next
+        if (pregate && i > 0 && blockIdx.x == 0)
+            for (int j = threadIdx.x; j < E; j += kStThreads) __stcg(a.acc_pg + (size_t)((i + 1) & 1) * E + j, 0ll);
+        cta_sync();
+        uint32_t *keys_t = reinterpret_cast<uint32_t *>(smem + C.o_sel);
+        if (threadIdx.x < 512) {
             // logit = rs * (W x) + bias: the RMSNorm scale applied to the summed dots
             uint32_t key = 0u;
             if (me < E) {
@@ -370,30 +411,48 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     if (a.logits_out) a.logits_out[(size_t)l * E + me] = lv;
                 }
             }
+            keys_t[(me & 15) * 32 + (me >> 4)] = key;
+        }
+        cta_sync();
+        // Warp 0 (outputs, miss count, flag) and the producer warp (expert copies) select, each
+        // on its own: the same code on the same keys gives the same selection and decisions.
+        // The other warps stage x_l meanwhile.
+        bool early = false;  // the producer warp issued the gate/up copies from its own selection
+        if (warp == 0 || warp == kStProducer) {
+            const int K = a.K;
             int my_id;
             float my_val;
-            uint64_t slot;
             {
-                uint8_t *sb = smem + C.o_sel;
-                cta_topk_thr<kStSelWarps>(key, a.table + (size_t)l * E, E, K, reinterpret_cast<uint32_t *>(sb),
-                                          reinterpret_cast<int *>(sb + 2048), reinterpret_cast<uint64_t *>(sb + 4096),
-                                          reinterpret_cast<uint32_t *>(sb + 8192), reinterpret_cast<int *>(sb + 8256),
-                                          reinterpret_cast<int *>(sb + 8320), my_id, my_val, slot);
+                uint8_t *ws = smem + C.o_sel + 2048 + warp * kStSelWarpBytes;
+                warp_topk_thr(keys_t, E, K, reinterpret_cast<uint32_t *>(ws), reinterpret_cast<int *>(ws + 128),
+                              reinterpret_cast<int *>(ws + 256), my_id, my_val);
+            }
+            uint64_t slot = 0;
+            if (tab_smem) {
+                if (!mbar_spin_warp(bar_tab, (uint32_t)(i & 1))) failed = true;
+                if (lane < K) slot = table_s[my_id];
+            } else if (lane < K) {
+                slot = __ldcg(a.table + (size_t)l * E + my_id);
+            }
+            // both warps take the same decisions from the same selection
+            const unsigned mmask = __ballot_sync(kFull, lane < K && slot == 0);
+            const int nmiss = __popc(mmask);
+            const bool bad = __ballot_sync(kFull, lane < K && slot != 0 && (slot & 15)) != 0;
+            // with fill tables, a miss whose record has a source is filled here by the device
+            // instead of stopping the launch
+            bool fillable = FILL && nmiss > 0;
+            if (FILL && fillable) {
+                const size_t at = (size_t)l * a.E + (lane < K ? my_id : 0);
+                const bool ok = !(lane < K && slot == 0) ||
+                                (a.fill_src[at] != 0 && a.fill_dst[at] != 0 && ((a.fill_src[at] | a.fill_dst[at]) & 15) == 0);
+                fillable = __all_sync(kFull, ok);
+            }
+            const bool stop = (nmiss > 0 && !fillable) || bad || flag0 <= l || failed;
+            if (warp == kStProducer && !stop && !(FILL && nmiss > 0)) {
+                issue_gu(__shfl_sync(kFull, slot, C.ka), __shfl_sync(kFull, slot, C.kb));
+                early = true;
             }
             if (warp == 0) {
-                const unsigned mmask = __ballot_sync(kFull, lane < K && slot == 0);
-                const int nmiss = __popc(mmask);
-                const bool bad = __ballot_sync(kFull, lane < K && slot != 0 && (slot & 15)) != 0;
-                // with fill tables, a miss whose record has a source is filled here by the device
-                // instead of stopping the launch
-                bool fillable = FILL && nmiss > 0;
-                if (FILL && fillable) {
-                    const size_t at = (size_t)l * a.E + (lane < K ? my_id : 0);
-                    const bool ok = !(lane < K && slot == 0) ||
-                                    (a.fill_src[at] != 0 && a.fill_dst[at] != 0 && ((a.fill_src[at] | a.fill_dst[at]) & 15) == 0);
-                    fillable = __all_sync(kFull, ok);
-                }
-                const bool stop = (nmiss > 0 && !fillable) || bad || flag0 <= l;
                 if (lane < K) {
                     slots_s[lane] = slot;
                     sv_s[lane] = my_val;
@@ -426,6 +485,25 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 if (lane == 0) *stop_s = stop;
             }
         }
+        {
+            float *x_s = reinterpret_cast<float *>(smem + C.o_x);
+            float4 *xt_s = reinterpret_cast<float4 *>(smem + C.o_xt);
+            // x_s in order; xt_s lane-transposed for the gate/up lanes: float4 q of the slice of
+            // lane L of row half h (columns h H/SPLIT + L 8 GPL ...) sits at [h][q][L ^ q] (the
+            // xor spreads the staging writes of consecutive q over the banks)
+#pragma unroll
+            for (int u = 0; u < kXv; ++u) {
+                const int j = threadIdx.x + u * kStThreads;
+                if (j >= H / 4) break;
+                const float4 v = xv_r[u];
+                reinterpret_cast<float4 *>(x_s)[j] = v;
+                const int hf = H / 4 / SPLIT, h = j / hf, r = j % hf, L = r / (2 * GPL), q = r % (2 * GPL);
+                xt_s[(h * 2 * GPL + q) * 32 + (L ^ q)] = v;
+            }
+        }
+        if (a.x_hist && blockIdx.x == 0)
+            for (int j = threadIdx.x; j < H; j += kStThreads) a.x_hist[(size_t)l * H + j] = __ldcg(a.x + j);
+        tab_pend = -1;
         cta_sync();
         if (*stop_s) break;
         if (FILL && *fmask_s) {
@@ -455,31 +533,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             }
             cta_sync();
         }
-        // the last warp issues the gate/up copies; the down rows and the next layer's router
-        // columns wait until the end of C, so that only the copies C needs first are queued
-        if (warp == kStProducer) {
-            fence_proxy_async_smem();
-            if (FILL) asm volatile("fence.proxy.async.global;" ::: "memory");  // records filled above
-            const int I = a.I, rowb = C.rowb;
-            const size_t matb = matrix_bytes(I, H);
-            // gate/up: lane i < 2 * kStGuChunks issues chunk (segment i / kStGuChunks, part
-            // i % kStGuChunks): its gate rows and its up rows, completion on bar_gu[i]
-            if (lane < 2 * kStGuChunks && C.p1 > C.p0) {
-                const int seg = lane / kStGuChunks, ch = lane % kStGuChunks;
-                const int n = seg == 0 ? C.n0 : C.n1;
-                const int r0 = gu_cut(C, U, seg, ch), r1 = gu_cut(C, U, seg, ch + 1);
-                if (r1 > r0) {
-                    const uint8_t *base = reinterpret_cast<const uint8_t *>(slots_s[seg == 0 ? C.ka : C.kb]);
-                    const int ia = seg == 0 ? C.p0 - C.ka * I : 0;
-                    const uint32_t bytes = (uint32_t)((r1 - r0) * rowb);
-                    uint8_t *gdst = smem + C.o_gu + (seg == 0 ? 0 : 2 * (size_t)C.n0 * rowb) + (size_t)r0 * rowb;
-                    mbar_arrive_expect_tx(&bar_gu[lane], 2 * bytes);
-                    bulk_g2s(gdst, base + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
-                    bulk_g2s(gdst + (size_t)n * rowb, base + matb + (size_t)(ia + r0) * rowb, bytes, &bar_gu[lane]);
-                }
-            }
-            if (lane == 0) *iss_s = 0;
-        }
+        // after a device fill the producer warp issues the gate/up copies from the new slots
+        if (warp == kStProducer && !early) issue_gu(slots_s[C.ka], slots_s[C.kb]);
         // the computing warps start once every copy is issued: issued under their load the
         // copies take about three times longer
         cta_sync();
@@ -566,14 +621,14 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             }
             if (threadIdx.x == kColThread) {
                 if (!last && nq > 0) issue_cols(i + 1);
-                if (!last && (E & 1) == 0 && (reinterpret_cast<uintptr_t>(a.table) & 15) == 0)  // 16-byte pieces
-                    prefetch_l2_bulk(a.table + (size_t)(l + 1) * E, (uint32_t)(E * sizeof(uint64_t)));
-                *iss_s = (nq > 0 ? 1 : 0) | (!last && nq > 0 ? 2 : 0);
+                if (!last && tab_smem) issue_tab(i + 1);  // the next layer's residency row
+                *iss_s = (nq > 0 ? 1 : 0) | (!last && nq > 0 ? 2 : 0) | (!last && tab_smem ? 4 : 0);
             }
             __syncwarp();
         }
         failed = cta_sync_or(failed) != 0;
         if (*iss_s & 2) rc_pend = i + 1;
+        if (*iss_s & 4) tab_pend = i + 1;
         if (failed) break;
         {
             const int p0 = C.p0, np = C.p1 - C.p0;
@@ -701,6 +756,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     // ---- exit: no copy into this CTA's shared memory may still be in flight ----
     if (threadIdx.x == 0) {
         if (rc_pend >= 0) mbar_wait(bar_rc, (uint32_t)(rc_pend & 1));
+        if (tab_pend >= 0) mbar_wait(bar_tab, (uint32_t)(tab_pend & 1));
         if (*iss_s & 1) mbar_wait(bar_dn, ph);
         if (ex_issued) {
             for (int bi = 0; bi < 2 * kStGuChunks; ++bi) {

@@ -248,6 +248,11 @@ rl_status moe_decode_static(const rl_moe_shape *shp, int32_t layer, const float 
  * it must be zero-filled again.  One CTA runs on every SM (cooperative launch); a shape whose
  * CTA does not fit an SM returns RL_ERR_UNSUPPORTED before any launch.  Every on-chip wait is
  * bounded: on expiry RL_DEVERR_WAIT_TIMEOUT is set in ctrl[1] and the launch ends.
+ * Bytes 64..71 of ws are test knobs and stay zero in normal use: the uint32 at byte 64, when
+ * nonzero, replaces the poll limit of every wait of the launch; the int32 at byte 68, n > 0,
+ * makes CTA n-1 leave before its first grid-barrier arrival, and n < 0 makes CTA -n-1 expect
+ * 16 bytes more than its first router-column copy brings, so that the other CTAs' waits run
+ * out (RL_DEVERR_WAIT_TIMEOUT) without any fault; zero-fill ws again afterwards.
  */
 size_t moe_decode_stack_workspace_bytes(const rl_moe_shape *shp);
 rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x, float norm_eps,

@@ -158,8 +158,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait for phase `parity` of an mbarrier; false when the cap ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitCap; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t cap = kWaitCap) {
+    for (uint32_t i = 0; i < cap; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
@@ -179,10 +179,10 @@ constexpr uint32_t kSpinPolls = 1u << 26;  // test_wait polls (tens of cycles ea
 // Bounded spin on test_wait by lane 0 of the warp (the other lanes park in __syncwarp): for
 // the hand-offs of a pipeline, where the wake-up delay of a suspended try_wait is too long.
 // Call with the whole warp; the result is warp-uniform.
-__device__ __forceinline__ bool mbar_spin_warp(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_spin_warp(uint64_t *bar, uint32_t parity, uint32_t cap = kSpinPolls) {
     int ok = 0;
     if ((threadIdx.x & 31) == 0) {
-        for (uint32_t i = 0; i < kSpinPolls; ++i)
+        for (uint32_t i = 0; i < cap; ++i)
             if (mbar_test_wait(bar, parity)) {
                 ok = 1;
                 break;
@@ -194,9 +194,9 @@ __device__ __forceinline__ bool mbar_spin_warp(uint64_t *bar, uint32_t parity) {
 // The same wait made by lane 0 of the warp alone while the other lanes park in __syncwarp, so
 // that a waiting warp does not keep the shared-memory pipe busy with polls (which slows the
 // warps that compute).  Call with the whole warp; the result is warp-uniform.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint32_t cap = kWaitCap) {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, cap) ? 1 : 0;
     __syncwarp();  // rejoin the warp (see cta_sync)
     return __shfl_sync(kFull, ok, 0) != 0;
 }

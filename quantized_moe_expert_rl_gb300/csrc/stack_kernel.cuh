@@ -53,6 +53,14 @@ constexpr int kStWarps = kStThreads / 32;
 constexpr int kStGuChunks = 2;
 constexpr int kStBars = 3 + 2 * kStGuChunks;  // [0] down rows, [1] router columns, [2..] gate/up chunks, [last] table row
 constexpr uint32_t kSpinCap = 1u << 22;       // global-memory polls (~1 us each): seconds
+// Test knobs in the workspace header (zero = off), so that a test can make the bounded waits
+// run out without faulting anything: the u32 at byte 64 replaces every wait limit of the
+// launch (polls of the grid barrier, of the copy barriers); the i32 at byte 68, when n > 0,
+// makes CTA n - 1 leave before its first grid-barrier arrival (the other CTAs' waits at that
+// barrier run out) and, when n < 0, makes CTA -n - 1 expect 16 bytes more than its first
+// router-column copy brings (its own wait on that copy runs out, the others then wait in vain
+// at the next grid barrier).
+constexpr int kStKnobWord = 16;  // u32 index of the knobs in the workspace header
 constexpr int kStSelWarps = 16;               // selection warps: E <= 32 * 16, one expert per thread
 constexpr int kStHdr = 1024;                  // barriers, scalars, CTA constants, outputs of the selection
 constexpr int kStPredMax = 32;                // experts prefetched on the pre-gated prediction
@@ -171,7 +179,7 @@ __device__ __forceinline__ float fixed_value(long long v) { return __ll2float_rn
 // Only the first arrival of a launch needs the counter's old value (to find the base); the
 // later ones are reductions that thread 0 does not wait for.
 __device__ __forceinline__ bool grid_sync(unsigned long long *ctr, unsigned long long &target, int *ok_s,
-                                          int32_t *ctrl) {
+                                          int32_t *ctrl, uint32_t cap) {
     cta_sync();
     if (threadIdx.x == 0) {
         if (target == 0ull) {
@@ -183,7 +191,7 @@ __device__ __forceinline__ bool grid_sync(unsigned long long *ctr, unsigned long
         }
         target += gridDim.x;
         bool ok = false;
-        for (uint32_t i = 0; i < kSpinCap; ++i)
+        for (uint32_t i = 0; i < cap; ++i)
             if (ld_acquire_u64(ctr) >= target - 1ull) {
                 ok = true;
                 break;
@@ -212,6 +220,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     int *stop_s = reinterpret_cast<int *>(smem + 68);
     int *ok_s = reinterpret_cast<int *>(smem + 72);
     int *iss_s = reinterpret_cast<int *>(smem + 76);  // copies issued at the end of C: bit 0 down rows, bit 1 router columns, bit 2 residency row
+    uint32_t *cap_s = reinterpret_cast<uint32_t *>(smem + 80);  // wait limits: grid barrier, copy spin, copy wait
+    int *hold_s = reinterpret_cast<int *>(smem + 92);           // test knob (see kStKnobWord)
     StCta &C = *reinterpret_cast<StCta *>(smem + 128);
     uint64_t *slots_s = reinterpret_cast<uint64_t *>(smem + 256);
     float *w_s = reinterpret_cast<float *>(smem + 384);   // [K] weights
@@ -250,6 +260,12 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         for (int i = 0; i < kStBars; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *iss_s = 0;
+        const uint32_t *knob = reinterpret_cast<const uint32_t *>(a.ctr) + kStKnobWord;
+        const uint32_t cap = __ldcg(knob);
+        cap_s[0] = cap ? cap : kSpinCap;
+        cap_s[1] = cap ? cap : kSpinPolls;
+        cap_s[2] = cap ? cap : kWaitCap;
+        *hold_s = (int)__ldcg(knob + 1);
     }
     build_pair_table(tab, a.codebook, nullptr);  // ends with __syncthreads
     const int flag0 = ld_ctrl(a.ctrl);
@@ -257,6 +273,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
 
     const int E = a.E;
     const int me = threadIdx.x;  // the router row (expert) whose columns this thread handles
+    const uint32_t cap_grid = cap_s[0], cap_spin = cap_s[1], cap_wait = cap_s[2];
+    const int hold = *hold_s;
     constexpr int kColThread = kStProducer * 32 + 31;  // issues the router column copies
     // Router columns [q0, q0 + dmax) of every row of layer index i (and of layer index i + 1
     // for the pre-gate dots) into shared memory: tensor copies of rc_rows(E) x dmax floats
@@ -264,7 +282,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     // They depend on nothing computed, so they are requested a layer ahead.
     auto issue_cols = [&](int i) {
         const int nb = (pregate && i + 1 < a.nl) ? 2 : 1, nbox = rc_nbox(E), rows = rc_rows(E);
-        mbar_arrive_expect_tx(bar_rc, (uint32_t)(nb * C.rcb));
+        const uint32_t extra = (i == 0 && hold == -(int)blockIdx.x - 1) ? 16u : 0u;  // test knob
+        mbar_arrive_expect_tx(bar_rc, (uint32_t)(nb * C.rcb) + extra);
         for (int q = 0; q < nb; ++q)
             for (int k = 0; k < nbox; ++k)
                 tma_load_2d(smem + C.o_rc + (size_t)q * C.rcb + (size_t)k * C.rbs, &a.wmap,
@@ -361,15 +380,16 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             __stcg(a.acc_pg + j, 0ll);
         }
     if ((int)threadIdx.x < C.nq) reinterpret_cast<float *>(smem + C.o_xq)[threadIdx.x] = __ldcg(a.x + C.q0 + threadIdx.x);
-    if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) failed = true;
+    if (hold == (int)blockIdx.x + 1) failed = true;  // test knob: this CTA never arrives
+    if (!failed && !grid_sync(a.ctr, target, ok_s, a.ctrl, cap_grid)) failed = true;
     if (!failed) {
-        if (warp == 0 && C.nq > 0 && !mbar_spin_warp(bar_rc, 0u)) failed = true;
+        if (warp == 0 && C.nq > 0 && !mbar_spin_warp(bar_rc, 0u, cap_spin)) failed = true;
         failed = cta_sync_or(failed) != 0;
     }
     if (!failed) {
         rc_pend = -1;
         add_partials(0);
-        if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) failed = true;
+        if (!grid_sync(a.ctr, target, ok_s, a.ctrl, cap_grid)) failed = true;
     }
     uint32_t ph = 0;
     for (int i = 0; !failed && i < a.nl; ++i, ph ^= 1u) {
@@ -429,7 +449,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             }
             uint64_t slot = 0;
             if (tab_smem) {
-                if (!mbar_spin_warp(bar_tab, (uint32_t)(i & 1))) failed = true;
+                if (!mbar_spin_warp(bar_tab, (uint32_t)(i & 1), cap_spin)) failed = true;
                 if (lane < K) slot = table_s[my_id];
             } else if (lane < K) {
                 slot = __ldcg(a.table + (size_t)l * E + my_id);
@@ -520,7 +540,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 uint4 *dp = reinterpret_cast<uint4 *>(a.fill_dst[at] + lo);
                 for (size_t j = threadIdx.x; j < (hi - lo) / 16; j += kStThreads) dp[j] = sp[j];
             }
-            if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
+            if (!grid_sync(a.ctr, target, ok_s, a.ctrl, cap_grid)) { failed = true; break; }
             if (threadIdx.x < (unsigned)a.K && ((fm >> threadIdx.x) & 1u)) {
                 const size_t at = (size_t)l * E + fid_s[threadIdx.x];
                 const uint64_t d = a.fill_dst[at];
@@ -570,7 +590,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 while (ch + 1 < kStGuChunks && r >= ((n / U) * (ch + 1) / kStGuChunks) * U) ++ch;
                 const int bi = seg * kStGuChunks + ch;
                 if (!(ready & (1u << bi))) {
-                    if (!mbar_wait_warp(&bar_gu[bi], ph)) to = true;
+                    if (!mbar_wait_warp(&bar_gu[bi], ph, cap_wait)) to = true;
                     ready |= 1u << bi;
                 }
                 gb = gtiles + (seg == 0 ? 0 : 2 * (size_t)n0 * rowb) + (size_t)r * rowb + boff;
@@ -635,7 +655,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             const float *part = reinterpret_cast<const float *>(smem + C.o_part);
             for (int t = threadIdx.x; t < np; t += kStThreads) __stcg(a.h + p0 + t, swiglu_part<SPLIT>(part + 4 * t));
         }
-        if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
+        if (!grid_sync(a.ctr, target, ok_s, a.ctrl, cap_grid)) { failed = true; break; }
 
         // ---------------- D: down rows of every expert, ordered combine, residual ----------------
         // acc[i & 1] was read by every CTA in B; it takes the sums of layer index i + 2 next
@@ -715,7 +735,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     const float4 v = h_s[q * LPR + (sl ^ q)];
                     hv[4 * q] = v.x; hv[4 * q + 1] = v.y; hv[4 * q + 2] = v.z; hv[4 * q + 3] = v.w;
                 }
-                if (trips > 0 && !mbar_wait_warp(bar_dn, ph)) {
+                if (trips > 0 && !mbar_wait_warp(bar_dn, ph, cap_wait)) {
                     failed = true;
                 } else {
                     const uint4 *tabc = tab + (lane & (kTabCopies - 1));
@@ -746,24 +766,27 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         }
         if (last) break;
         // the next layer's router dots on this CTA's slice of x_{l+1}
-        if (warp == 0 && C.nq > 0 && !mbar_spin_warp(bar_rc, (uint32_t)((i + 1) & 1))) failed = true;
+        if (warp == 0 && C.nq > 0 && !mbar_spin_warp(bar_rc, (uint32_t)((i + 1) & 1), cap_spin)) failed = true;
         failed = cta_sync_or(failed) != 0;
         if (failed) break;
         rc_pend = -1;
         add_partials(i + 1);
-        if (!grid_sync(a.ctr, target, ok_s, a.ctrl)) { failed = true; break; }
+        if (!grid_sync(a.ctr, target, ok_s, a.ctrl, cap_grid)) { failed = true; break; }
     }
     // ---- exit: no copy into this CTA's shared memory may still be in flight ----
     if (threadIdx.x == 0) {
-        if (rc_pend >= 0) mbar_wait(bar_rc, (uint32_t)(rc_pend & 1));
-        if (tab_pend >= 0) mbar_wait(bar_tab, (uint32_t)(tab_pend & 1));
-        if (*iss_s & 1) mbar_wait(bar_dn, ph);
+        bool drained = true;
+        if (rc_pend >= 0) drained &= mbar_wait(bar_rc, (uint32_t)(rc_pend & 1), cap_wait);
+        if (tab_pend >= 0) drained &= mbar_wait(bar_tab, (uint32_t)(tab_pend & 1), cap_wait);
+        if (*iss_s & 1) drained &= mbar_wait(bar_dn, ph, cap_wait);
         if (ex_issued) {
             for (int bi = 0; bi < 2 * kStGuChunks; ++bi) {
                 const int seg = bi / kStGuChunks, ch = bi % kStGuChunks;
-                if (C.p1 > C.p0 && gu_cut(C, U, seg, ch + 1) > gu_cut(C, U, seg, ch)) mbar_wait(&bar_gu[bi], ph);
+                if (C.p1 > C.p0 && gu_cut(C, U, seg, ch + 1) > gu_cut(C, U, seg, ch))
+                    drained &= mbar_wait(&bar_gu[bi], ph, cap_wait);
             }
         }
+        if (!drained) dev_error(a.ctrl, RL_DEVERR_WAIT_TIMEOUT);
     }
     cta_sync();
 }

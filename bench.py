@@ -397,43 +397,7 @@ def run_ours(a):
                     "us_per_layer": t_launch * 1e6 / model.L, "peak_source": f"{peak_kind} hbm_gbs"}
     else:
         # ---- dominant call: moe_decode (expert gate/up GEMV + down GEMV with ordered combine) ----
-        # Timed alone per launch with events on its stream, over sampled tokens x all layers, the
-        # slots of each (token, layer) recorded first from the real chain.
-        slots_rec = torch.zeros((kt_tokens, model.L, w.top_k), dtype=torch.int64, device=dev)
-        w_rec = torch.zeros((kt_tokens, model.L, w.top_k), dtype=torch.float32, device=dev)
-        xs_rec = torch.zeros((kt_tokens, model.L, w.hidden), dtype=torch.float32, device=dev)
-        with torch.cuda.stream(stream):
-            for t in range(kt_tokens):
-                engine.enqueue_decode_token(model, b, x_in[t], y_out[t], stacked, x_hist=xs_rec[t] if stacked else None)
-                slots_rec[t].copy_(b.slots)
-                w_rec[t].copy_(b.weights)
-                if not stacked:
-                    xs_rec[t, 0].copy_(x_in[t])
-        stream.synchronize()
-        ybuf = torch.zeros(w.hidden, dtype=torch.float32, device=dev)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(kt_tokens * model.L)]
-        eps = engine.EPS if stacked else -1.0
-        with torch.cuda.stream(stream):
-            for rep in range(2):                      # first pass warms the code path
-                i = 0
-                for t in range(kt_tokens):
-                    for l in range(model.L):
-                        s_, e_ = evs[i]
-                        s_.record(stream)
-                        L.moe_decode(model.shape, l, xs_rec[t, l], eps, slots_rec[t, l], w_rec[t, l],
-                                     model.codebook, ybuf, 0, b.ctrl, b.dec_ws, b.dec_ws.numel(), stream)
-                        e_.record(stream)
-                        i += 1
-        stream.synchronize()
-        durs = np.array([s_.elapsed_time(e_) for s_, e_ in evs]) * 1e-3      # seconds
-        t_launch = float(np.mean(durs))
-        bytes_per_launch = (w.top_k * w.record_bytes + 2 * w.hidden * 4 + 2 * w.top_k * w.inter * 4)
-        achieved = bytes_per_launch / t_launch / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": _traffic("moe_decode", 1.0), "kernel": "moe_decode (gate/up + down GEMVs)",
-                    "bytes_per_launch": bytes_per_launch, "launch_us": t_launch * 1e6,
-                    "peak_source": f"{peak_kind} hbm_gbs"}
+        roofline = moe_decode_roofline(model, b, x_in, stacked, kt_tokens, stream, dev)
 
     line = None
     if rank == 0:
@@ -441,6 +405,8 @@ def run_ours(a):
         if ws == 1 and not a.no_cpu_baseline:
             rate, cores, sample = oracle_rate(a.workload, budget_s=a.cpu_budget_s)
             cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+            rate1, _, sample1 = oracle_rate(a.workload, budget_s=a.cpu_budget_s / 2, cores=1)
+            cpu["single_thread"] = {"value": rate1, "unit": "tokens/s", "cores": 1, "sample": sample1}
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": a.steps,
                 "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -453,6 +419,12 @@ def run_ours(a):
         if ws == 1 and not a.no_prefill:
             del model
             torch.cuda.empty_cache()
+            if a.workload == "decode_stack":
+                line["decode_layer"] = decode_layer_leg(dev, max(1, a.steps // 3), 3)
+                torch.cuda.empty_cache()
+                if not a.no_bounded:
+                    line["decode_bounded"] = bounded_decode_leg(dev)
+                    torch.cuda.empty_cache()
             line["prefill"] = prefill_leg(dev, a.steps, a.warmup)
             if not a.no_bounded:
                 torch.cuda.empty_cache()
@@ -461,6 +433,147 @@ def run_ours(a):
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def moe_decode_roofline(model, b, x_in, stacked: bool, kt_tokens: int, stream, dev) -> dict:
+    """moe_decode (expert gate/up GEMV + down GEMV with ordered combine) timed alone per call
+    with events on its stream, over kt_tokens sampled tokens x all layers; the slots, weights
+    and layer inputs of each (token, layer) are recorded first from the real chain."""
+    import numpy as np
+    import torch
+
+    from quantized_moe_expert_rl_gb300 import _lib as L
+    from quantized_moe_expert_rl_gb300 import engine
+    w = model.w
+    slots_rec = torch.zeros((kt_tokens, model.L, w.top_k), dtype=torch.int64, device=dev)
+    w_rec = torch.zeros((kt_tokens, model.L, w.top_k), dtype=torch.float32, device=dev)
+    xs_rec = torch.zeros((kt_tokens, model.L, w.hidden), dtype=torch.float32, device=dev)
+    yscr = torch.zeros(w.hidden, dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        for t in range(kt_tokens):
+            engine.enqueue_decode_token(model, b, x_in[t], yscr, stacked, x_hist=xs_rec[t] if stacked else None)
+            slots_rec[t].copy_(b.slots)
+            w_rec[t].copy_(b.weights)
+            if not stacked:
+                xs_rec[t, 0].copy_(x_in[t])
+    stream.synchronize()
+    ybuf = torch.zeros(w.hidden, dtype=torch.float32, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(kt_tokens * model.L)]
+    eps = engine.EPS if stacked else -1.0
+    with torch.cuda.stream(stream):
+        for rep in range(2):                      # first pass warms the code path
+            i = 0
+            for t in range(kt_tokens):
+                for l in range(model.L):
+                    s_, e_ = evs[i]
+                    s_.record(stream)
+                    L.moe_decode(model.shape, l, xs_rec[t, l], eps, slots_rec[t, l], w_rec[t, l],
+                                 model.codebook, ybuf, 0, b.ctrl, b.dec_ws, b.dec_ws.numel(), stream)
+                    e_.record(stream)
+                    i += 1
+    stream.synchronize()
+    durs = np.array([s_.elapsed_time(e_) for s_, e_ in evs]) * 1e-3      # seconds
+    t_launch = float(np.mean(durs))
+    bytes_per_launch = (w.top_k * w.record_bytes + 2 * w.hidden * 4 + 2 * w.top_k * w.inter * 4)
+    achieved = bytes_per_launch / t_launch / 1e9
+    peak, peak_kind = _peaks()
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": _traffic("moe_decode", 1.0), "kernel": "moe_decode (gate/up + down GEMVs)",
+            "bytes_per_launch": bytes_per_launch, "launch_us": t_launch * 1e6,
+            "peak_source": f"{peak_kind} hbm_gbs"}
+
+
+def decode_layer_leg(dev, steps: int, warmup: int) -> dict:
+    """Single-token decode of one layer (hidden 2048, 512 experts, top-10, inter 512): 1000
+    seeded tokens, one at a time, each one CUDA graph of rl_route + moe_decode (y = MoE(x), no
+    norm, no residual); moe_decode also timed alone per call against the HBM roofline."""
+    import torch
+
+    import synth
+    from quantized_moe_expert_rl_gb300 import engine
+    w = synth.WORKLOADS["decode_layer"]
+    model = engine.Model(w, device=dev)
+    b = engine.DecodeBuffers.make(model)
+    T = w.tokens
+    x = torch.from_numpy(synth.tokens(w, 0, T)).to(dev)
+    y = torch.zeros_like(x)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        engine.enqueue_decode_token(model, b, x[0], y[0], False)
+    stream.synchronize()
+    graphs = []
+    for t in range(T):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            engine.enqueue_decode_token(model, b, x[t], y[t], False)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            for g in graphs:
+                g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            for g in graphs:
+                g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    roof = moe_decode_roofline(model, b, x, False, 16, stream, dev)
+    ctrl = b.ctrl.cpu().tolist()
+    assert ctrl == [0x7FFFFFFF, 0], ctrl
+    return {"workload": "decode_layer (1 layer, 1000 tokens one at a time)",
+            "path": "per-token CUDA graph: rl_route + moe_decode (3 kernels)",
+            "tokens_per_s": T / (ms * 1e-3), "us_per_token": ms * 1e3 / T, "roofline": roof,
+            "target": "expert GEMVs at >= 70% of HBM peak"}
+
+
+def bounded_decode_leg(dev, n_tokens: int = 16) -> dict:
+    """The decode stack with bounded residency at full shape: 48 layers x 512 experts, 435 of
+    them resident per layer (seeded), the first n_tokens seeded tokens from that residency.
+    Device path: one moe_decode_stack_fill launch per token (absent experts copied by the GPU
+    from the pinned backing store inside the launch); host path: the stack stops at each layer
+    that selects an absent expert, the host fills and the stack resumes."""
+    import time
+    from dataclasses import replace
+
+    import torch
+
+    import synth
+    from quantized_moe_expert_rl_gb300 import engine
+    w = replace(synth.WORKLOADS["decode_stack"], n_resident=435)
+    model = engine.Model(w, device=dev)
+    b = engine.DecodeBuffers.make(model)
+    x = torch.from_numpy(synth.tokens(w, 0, n_tokens)).to(dev)
+    y = torch.zeros_like(x)
+    res = {}
+    for mode in ("device", "host"):
+        model.reset_residency()
+        filled = torch.zeros(1, dtype=torch.int32, device=dev)
+        stops = fills = misses = 0
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for t in range(n_tokens):
+            b.miss.zero_()
+            if mode == "device":
+                engine.run_bounded_decode_token_device(model, b, x[t], y[t], filled)
+            else:
+                st = engine.run_bounded_decode_token(model, b, x[t], y[t])
+                stops += len(st.early_outs)
+                fills += len(st.filled)
+            misses += int(b.miss.sum().item())
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        if mode == "device":
+            fills = int(filled.item())
+        assert b.ctrl.cpu().tolist() == [0x7FFFFFFF, 0]
+        res[mode] = {"tokens_per_s": n_tokens / wall, "ms_per_token": wall * 1e3 / n_tokens,
+                     "experts_filled": fills, "misses": misses}
+        if mode == "host":
+            res[mode]["stops"] = stops
+    return {"workload": f"decode_stack with 435/512 experts resident per layer, first {n_tokens} tokens "
+                        f"from the seeded residency", **res}
 
 
 def prefill_leg(dev, steps: int, warmup: int, path: str = "tc"):
@@ -526,6 +639,7 @@ def bounded_leg(dev, steps: int, warmup: int, path: str = "tc"):
     chunk from the seeded residency (fills from pinned host memory on each early-out)."""
     import time
 
+    import numpy as np
     import torch
 
     import synth
@@ -563,6 +677,28 @@ def bounded_leg(dev, steps: int, warmup: int, path: str = "tc"):
             dwalls.append(time.perf_counter() - t0)
             dlast = dst
     dwall = sum(dwalls) / len(dwalls)
+    # one more device-filled chunk with every stage timed by events, the routing of every
+    # layer kept to count the distinct experts each layer runs
+    model.reset_residency()
+    x.copy_(x0)
+    ids_hist = torch.zeros((model.L, w.tokens, w.top_k), dtype=torch.int32, device=dev)
+    split = {}
+    engine.run_bounded_chunk_device(model, b, x, path=path, hist={"ids": ids_hist}, timing=split)
+    ids_np = ids_hist.cpu().numpy()
+    union = sum(len(np.unique(ids_np[l])) for l in range(model.L))
+    P = w.tokens * w.top_k
+    flops = model.L * 2.0 * P * 3 * w.hidden * w.inter
+    wbytes = union * w.record_bytes
+    t_ex = split["experts"] * 1e-3
+    hbm, hbm_kind = _peaks()
+    tf, tf_kind = _tensor_peak()
+    t_hbm, t_tc = wbytes / (hbm * 1e9), flops / (tf * 1e12)
+    roof = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "kernel": f"moe_prefill_chunk over the {model.L} layers (pair build + grouped tc_gemm)",
+            "achieved_tflops": flops / t_ex / 1e12, "peak_tflops": tf, "frac_tensor": t_tc / t_ex,
+            "achieved_gbs": wbytes / t_ex / 1e9, "peak_gbs": hbm, "frac_hbm": t_hbm / t_ex,
+            "flop_per_chunk": flops, "weight_bytes_per_chunk": wbytes, "union_experts": union,
+            "peak_source": f"{hbm_kind} hbm_gbs, {tf_kind}"}
     return {"workload": "prefill_bounded (48 layers x 2048 tokens, Zipf 1.1, 435/512 resident)",
             "tokens_per_s_excl_fill": w.tokens / (wall - fill), "tokens_per_s_incl_fill": w.tokens / wall,
             "s_per_chunk": wall, "fill_s_per_chunk": fill, "early_outs": len(last.early_outs),
@@ -570,7 +706,9 @@ def bounded_leg(dev, steps: int, warmup: int, path: str = "tc"):
             "experts_filled": len(last.filled), "fill_bytes": last.fill_bytes, "host_syncs": last.syncs,
             "device_fill": {"tokens_per_s": w.tokens / dwall, "s_per_chunk": dwall,
                             "experts_filled": len(dlast.filled), "misses_total": sum(dlast.miss),
-                            "host_syncs": dlast.syncs}}
+                            "host_syncs": dlast.syncs,
+                            "split_ms": {k: round(v, 3) for k, v in split.items()},
+                            "roofline": roof}}
 
 
 def main():

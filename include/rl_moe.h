@@ -79,7 +79,9 @@ typedef enum rl_status {
 #define RL_DEVERR_WAIT_TIMEOUT 2 /* a bounded on-chip wait ran out of iterations */
 #define RL_DEVERR_BAD_ID 4       /* an expert id outside [0, n_experts) was read */
 #define RL_DEVERR_MISSING 8      /* an expert kernel met a zero (absent) slot */
-#define RL_DEVERR_RANGE 16       /* moe_decode_stack: a router partial sum outside the fixed-point range */
+#define RL_DEVERR_RANGE 16       /* a fixed-point sum met a term outside its range: a router partial
+                                    (moe_decode_stack) or a group of 8 squares of the RMSNorm
+                                    (|x| beyond about 1400; rl_route, moe_decode, moe_decode_stack) */
 #define RL_DEVERR_NAN 32         /* a router logit was NaN; NaN ranks below every number (never
                                     selected while K numbers remain), so inputs holding NaN
                                     are refused through this bit */
@@ -102,9 +104,14 @@ size_t rl_record_bytes(const rl_moe_shape *shp);
 /*
  * rl_rmsnorm - unit-gain RMSNorm of T rows of width H:
  *   xn[t][h] = x[t][h] * r_t,  r_t = 1 / sqrt(mean_h(x[t][h]^2) + eps), computed in f32.
- * x, xn: [T][H] f32 row-major, 16-byte aligned (may alias).  H a multiple of 128; T >= 0.
- * The scale r_t is computed with one fixed summation order; rl_route and moe_decode compute
- * the very same r_t when they normalise their input on the fly (norm_eps >= 0).
+ * x, xn: [T][H] f32 row-major, 16-byte aligned (may alias).  H a multiple of 256; T >= 0.
+ * mean(x^2) is summed exactly and in no particular order: the squares of each group of 8
+ * consecutive values are added in a fixed f32 tree, each group sum is rounded to a multiple of
+ * 2^-30 and the groups are added as 64-bit integers.  rl_route, moe_decode and
+ * moe_decode_stack (which adds the groups of its CTAs' slices of x) compute the very same r_t
+ * when they normalise their input on the fly (norm_eps >= 0).  A group sum of 2^25 or more
+ * (|x| beyond about 1400) counts as 2^25; the calls with a control block then set
+ * RL_DEVERR_RANGE.
  */
 rl_status rl_rmsnorm(const float *x, float *xn, int32_t T, int32_t H, float eps, void *stream);
 

@@ -115,8 +115,12 @@ __global__ void __launch_bounds__(kGuThreads) dec_gateup_kernel(const float *__r
     cta_sync();  // x staged, ok_s written; warp 0 rejoined after its lane-dependent copy issue
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (NORM && warp == 0) {
-        const float r = rms_scale_warp(x_s, H, eps);
-        if (lane == 0) *scale_s = r;
+        bool range = false;
+        const float r = rms_scale_warp(x_s, H, eps, &range);
+        if (lane == 0) {
+            *scale_s = r;
+            if (range && blockIdx.x == 0) dev_error(ctrl, RL_DEVERR_RANGE);
+        }
     }
     cta_sync();
     if (!*ok_s) return;

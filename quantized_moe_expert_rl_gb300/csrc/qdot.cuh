@@ -99,18 +99,67 @@ __device__ __forceinline__ unsigned long long group_fma(uint32_t gs, const unsig
     return acc;
 }
 
-// Deterministic RMSNorm scale 1/sqrt(mean(x^2) + eps) of H values, computed by ONE warp with a
-// fixed summation order (identical in every kernel that calls it, so every kernel sees the
-// same normalised input).  Returns the scale in every lane.
-__device__ __forceinline__ float rms_scale_warp(const float *__restrict__ x, int H, float eps) {
-    const int lane = threadIdx.x & 31;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    for (int c = lane * 4; c < H; c += 128) {
-        const float4 v = *reinterpret_cast<const float4 *>(x + c);
-        a0 = fmaf(v.x, v.x, a0); a1 = fmaf(v.y, v.y, a1); a2 = fmaf(v.z, v.z, a2); a3 = fmaf(v.w, v.w, a3);
+// RMSNorm scale 1/sqrt(mean(x^2) + eps) with an exact, order-free sum of squares, so that
+// every kernel that normalises a row (whole or split between CTAs) gets the same bits.  The
+// squares of each group of 8 consecutive values are added in the fixed tree
+// ((x0^2 + x1^2) + (x2^2 + x3^2)) + ((x4^2 + x5^2) + (x6^2 + x7^2)) in f32 without
+// contraction; each group sum is rounded to a multiple of 2^-30 and the groups are added as
+// 64-bit integers (exact, so any split of the groups gives the same total).  A group sum at or
+// above 2^25 (|x| beyond about 1400) or NaN is outside the range: it counts as 2^25 and the
+// caller is told (RL_DEVERR_RANGE where it has a control block).
+constexpr float kSqScale = 1073741824.0f;          // 2^30
+constexpr float kSqInv = 9.313225746154785e-10f;   // 2^-30
+constexpr float kSqMax = 33554432.0f;              // 2^25
+
+__device__ __forceinline__ float sq8(float4 a, float4 b) {
+    const float p = __fadd_rn(__fadd_rn(__fmul_rn(a.x, a.x), __fmul_rn(a.y, a.y)),
+                              __fadd_rn(__fmul_rn(a.z, a.z), __fmul_rn(a.w, a.w)));
+    const float q = __fadd_rn(__fadd_rn(__fmul_rn(b.x, b.x), __fmul_rn(b.y, b.y)),
+                              __fadd_rn(__fmul_rn(b.z, b.z), __fmul_rn(b.w, b.w)));
+    return __fadd_rn(p, q);
+}
+// The same group sum when lane t of an aligned group of 8 lanes holds value t: the shuffle
+// tree pairs the same terms (and f32 addition is commutative), so every lane of the group
+// returns sq8's bits.  Call with the whole warp.
+__device__ __forceinline__ float sq8_lanes(float v) {
+    float s = __fmul_rn(v, v);
+    s = __fadd_rn(s, __shfl_xor_sync(kFull, s, 1));
+    s = __fadd_rn(s, __shfl_xor_sync(kFull, s, 2));
+    s = __fadd_rn(s, __shfl_xor_sync(kFull, s, 4));
+    return s;
+}
+__device__ __forceinline__ long long sq_fixed(float s, bool &range) {
+    if (!(s < kSqMax)) {
+        range = true;
+        s = kSqMax;
     }
-    float ss = warp_sum((a0 + a1) + (a2 + a3));
-    return 1.0f / sqrtf(ss / (float)H + eps);
+    return float_to_ll(s * kSqScale);
+}
+__device__ __forceinline__ float rms_scale_from(long long ss, int H, float eps) {
+    return 1.0f / sqrtf(ll_to_float(ss) * kSqInv / (float)H + eps);
+}
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// The scale of H values (H a multiple of 256) by ONE warp: lane L takes the groups L, L + 32,
+// ...  Returns the scale in every lane; *range (optional) is set in every lane when a group
+// was out of range.
+__device__ __forceinline__ float rms_scale_warp(const float *__restrict__ x, int H, float eps, bool *range = nullptr) {
+    const int lane = threadIdx.x & 31;
+    long long acc = 0;
+    bool rg = false;
+    for (int g = lane; g < H / 8; g += 32) {
+        const float4 a = *reinterpret_cast<const float4 *>(x + 8 * g);
+        const float4 b = *reinterpret_cast<const float4 *>(x + 8 * g + 4);
+        acc += sq_fixed(sq8(a, b), rg);
+    }
+    acc = warp_sum_ll(acc);
+    const bool any = __any_sync(kFull, rg);
+    if (range) *range = any;
+    return rms_scale_from(acc, H, eps);
 }
 
 // ---- programmatic dependent launch ---------------------------------------------------------

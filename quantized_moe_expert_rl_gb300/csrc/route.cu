@@ -74,8 +74,12 @@ __global__ void __launch_bounds__(kR1Threads) route1_kernel(const float *__restr
 #pragma unroll
         for (int j = 0; j < NV; ++j) xv[j] = reinterpret_cast<const float4 *>(x)[lane + 32 * j];
         if (NORM && warp == 0) {
-            const float r = rms_scale_warp(x, H, eps);
-            if (lane == 0) *scale_s = r;
+            bool range = false;
+            const float r = rms_scale_warp(x, H, eps, &range);
+            if (lane == 0) {
+                *scale_s = r;
+                if (range && blockIdx.x == 0) dev_error(ctrl, RL_DEVERR_RANGE);
+            }
         }
     }
     cta_sync();
@@ -289,7 +293,7 @@ static rl_status launch_route1_n(bool norm, const float *x, float eps, const flo
 using namespace rl;
 
 extern "C" rl_status rl_rmsnorm(const float *x, float *xn, int32_t T, int32_t H, float eps, void *stream) {
-    if (T < 0 || H <= 0 || (H % 128)) return fail(RL_ERR_INVALID, "rl_rmsnorm: bad T=%d or H=%d", T, H);
+    if (T < 0 || H <= 0 || (H % 256)) return fail(RL_ERR_INVALID, "rl_rmsnorm: bad T=%d or H=%d (H a multiple of 256)", T, H);
     if (!(eps >= 0.f)) return fail(RL_ERR_INVALID, "rl_rmsnorm: eps must be >= 0");
     if (T == 0) return RL_OK;  // no rows: the buffers are not read (they may be NULL)
     if (!x || !xn) return fail(RL_ERR_INVALID, "rl_rmsnorm: NULL buffer");

@@ -27,19 +27,17 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// After the call lane r < K holds the r-th selected expert (my_id) and its logit (my_val).
-// key_of(e) gives the key of expert e (0 for an absent one), for e < 32 * C.  K <= MAXK <= 32.
-template <int C, int MAXK = kMaxK, class KeyOf>
-__device__ __forceinline__ void warp_topk_by(KeyOf key_of, int K, int &my_id, float &my_val) {
+// The rounds of the selection on keys already in registers: key[i] is the key of expert
+// lane * C + i (0 for an absent one).  After the call lane r < K holds the r-th selected expert
+// (my_id) and its logit (my_val).  K <= MAXK <= 32.  Consumes `key`.
+template <int C, int MAXK = kMaxK>
+__device__ __forceinline__ void warp_topk_keys(uint32_t (&key)[C], int K, int &my_id, float &my_val) {
     const int lane = threadIdx.x & 31;
-    uint32_t key[C];
     uint32_t best = 0u;
     int bi = 0;
 #pragma unroll
-    for (int i = 0; i < C; ++i) {
-        key[i] = key_of(lane * C + i);
+    for (int i = 0; i < C; ++i)
         if (key[i] > best) { best = key[i]; bi = i; }
-    }
     my_id = 0;
     my_val = 0.f;
 #pragma unroll
@@ -60,6 +58,16 @@ __device__ __forceinline__ void warp_topk_by(KeyOf key_of, int K, int &my_id, fl
         }
         __syncwarp();  // rejoin before the next round's votes (see cta_sync)
     }
+}
+
+// The same with the keys given by key_of(e) for e < 32 * C.
+template <int C, int MAXK = kMaxK, class KeyOf>
+__device__ __forceinline__ void warp_topk_by(KeyOf key_of, int K, int &my_id, float &my_val) {
+    const int lane = threadIdx.x & 31;
+    uint32_t key[C];
+#pragma unroll
+    for (int i = 0; i < C; ++i) key[i] = key_of(lane * C + i);
+    warp_topk_keys<C, MAXK>(key, K, my_id, my_val);
 }
 
 // warp_topk_by on E logits read through L2 (they may come from other CTAs); true in every lane
@@ -129,170 +137,104 @@ __device__ __forceinline__ bool precedes(uint32_t ka, int ia, uint32_t kb, int i
     return ka > kb || (ka == kb && ia < ib);
 }
 
-// Top-k of up to 32 * NW logits with NW warps of one CTA (the fused decode stack runs it in
-// every CTA), in few dependent steps.  Thread 32w + lane passes `key`, the key of expert
-// 32w + lane (0 when absent; the threads of warps >= NW pass 0).  Let m_w be
-// the largest key of warp w and T the K-th largest of the m_w: the
-// K warps holding the K largest maxima give K keys >= T, so the K-th largest key overall is
-// >= T and every key of the top-K is >= T.  The keys >= T (usually a few tens) are gathered and
-// each is ranked exactly against the others in the order (logit descending, index ascending);
-// the K first are the selection, the same as warp_topk's.  cand_*: shared scratch of 32 * NW
-// entries; wm_s: NW words; sel: K entries; cnt_s: one word.  Lane r < K of every warp ends
-// with the r-th selection; the CTA is converged on return.  K <= NW.
-template <int NW>
-__device__ __forceinline__ void cta_topk_thr(uint32_t key, const uint64_t *__restrict__ table_row, int E, int K,
-                                             uint32_t *cand_key, int *cand_id, uint64_t *cand_slot,
-                                             uint32_t *wm_s, int *sel, int *cnt_s, int &my_id, float &my_val,
-                                             uint64_t &my_slot) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int e = warp * 32 + lane;
-    if (warp >= NW || e >= E) key = 0u;
-    if (threadIdx.x == 0) *cnt_s = 0;
-    if (warp < NW) {
-        const uint32_t m = __reduce_max_sync(kFull, key);
-        if (lane == 0) wm_s[warp] = m;
-    }
-    cta_sync();
-    if (warp < NW) {
-        // T = the K-th largest warp maximum (ties by warp index, which only fixes who holds it)
-        const uint32_t mj = lane < NW ? wm_s[lane] : 0u;
-        int rank = 0;
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            const uint32_t mi = wm_s[i];
-            rank += (mi > mj || (mi == mj && i < lane)) ? 1 : 0;
-        }
-        const int who = __ffs(__ballot_sync(kFull, lane < NW && rank == K - 1)) - 1;
-        const uint32_t T = __shfl_sync(kFull, mj, who);
-        const bool cand = e < E && key >= T;
-        const unsigned mask = __ballot_sync(kFull, cand);
-        int base = 0;
-        if (lane == 0 && mask) base = atomicAdd(cnt_s, __popc(mask));
-        __syncwarp();
-        base = __shfl_sync(kFull, base, 0);
-        if (cand) {
-            const int at = base + __popc(mask & ((1u << lane) - 1u));
-            cand_key[at] = key;
-            cand_id[at] = e;
-            cand_slot[at] = __ldcg(table_row + e);
-        }
-    }
-    cta_sync();
-    const int n = *cnt_s;
-    for (int c = threadIdx.x; c < n; c += blockDim.x) {
-        const uint32_t kc = cand_key[c];
-        const int ic = cand_id[c];
-        int r = 0;
-#pragma unroll 4
-        for (int j = 0; j < n; ++j) r += precedes(cand_key[j], cand_id[j], kc, ic) ? 1 : 0;
-        if (r < K) sel[r] = c;
-    }
-    cta_sync();
-    my_id = 0;
-    my_val = 0.f;
-    my_slot = 0;
-    if (lane < K) {
-        const int c = sel[lane];
-        my_id = cand_id[c];
-        my_val = key_value(cand_key[c]);
-        my_slot = cand_slot[c];
-    }
-    __syncwarp();
-}
-
 }  // namespace rl
 
 namespace rl {
 
-// Top-k of up to 512 keys by ONE warp, in a few dependent steps, so that every warp of a CTA
-// can select on its own with no CTA barrier after the keys are written.  keys_t holds the key
-// of expert e at [(e % 16) * 32 + e / 16] (0 for absent experts and for e >= E), so lane L
-// reads the keys of experts 16 L .. 16 L + 15 with conflict-free loads and lower lanes hold
-// lower indices.  Let m_L be lane L's largest key and T the K-th largest of the 32 m_L: the K
-// lanes holding the K largest give K keys >= T, so every key of the top-K is >= T.  The keys
-// >= T (a few tens at most, usually) are gathered into the warp's scratch and each is ranked
-// exactly against the others in the order (logit descending, index ascending); with more than
-// 32 candidates (heavy ties) K rounds of warp arg-max take over.  The selection equals
-// warp_topk's.  Scratch: ck[32], ci[32], sel[kMaxK] of this warp.  Lane r < K ends with the
-// r-th selection; the warp is converged on return.
-__device__ __forceinline__ void warp_topk_thr(const uint32_t *keys_t, int E, int K, uint32_t *ck, int *ci, int *sel,
-                                              int &my_id, float &my_val) {
+// Expert of key j of a lane in the layout the fused decode loads its logit accumulators in:
+// chunk c = j / 2 covers experts [64 c, 64 c + 64), lane L holds experts 64 c + 2 L and
+// 64 c + 2 L + 1 (one 16-byte load per lane and chunk, the warp's load contiguous), so that
+// every CTA reads each 32-byte sector of the accumulators once.
+__device__ __forceinline__ int sel_id(int lane, int j) { return 64 * (j >> 1) + 2 * lane + (j & 1); }
+
+// Top-k of up to 512 keys by ONE warp from registers, in a few dependent steps: k[j] is the
+// key of expert sel_id(lane, j) (0 for an absent expert and for ids >= E).  Let m_L be lane L's
+// largest key and T the K-th largest of the 32 m_L: the K lanes holding the K largest give K
+// keys >= T, so every key of the top-K is >= T.  The keys >= T (a few tens at most, usually)
+// are gathered into the warp's scratch and each is ranked exactly against the others in the
+// order (logit descending, index ascending); with more than 32 candidates (heavy ties) K
+// rounds of exact warp arg-max over (key, index) take over.  The selection equals warp_topk's.
+// The all-to-all comparisons read shared memory by broadcast (every lane the same word), not
+// shuffles.  Scratch (this warp's, 8-byte aligned): wm[32] lane maxima, cand[32] (key, id)
+// pairs, sel[kMaxK].  Lane r < K ends with the r-th selection; the warp is converged on return.
+__device__ __forceinline__ void warp_topk_thr(const uint32_t (&k)[16], int E, int K, uint32_t *wm, uint2 *cand,
+                                              int *sel, int &my_id, float &my_val) {
     const int lane = threadIdx.x & 31;
-    uint32_t k[16];
     uint32_t m = 0u;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        k[j] = keys_t[j * 32 + lane];
-        m = k[j] > m ? k[j] : m;
-    }
+    for (int j = 0; j < 16; ++j) m = k[j] > m ? k[j] : m;
+    wm[lane] = m;
+    __syncwarp();
     int rank = 0;  // rank of m among the lane maxima (ties by lane)
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const uint32_t mj = __shfl_sync(kFull, m, j);
-        rank += (mj > m || (mj == m && j < lane)) ? 1 : 0;
+    for (int q = 0; q < 8; ++q) {
+        const uint4 v = reinterpret_cast<const uint4 *>(wm)[q];
+        rank += (v.x > m || (v.x == m && 4 * q + 0 < lane)) ? 1 : 0;
+        rank += (v.y > m || (v.y == m && 4 * q + 1 < lane)) ? 1 : 0;
+        rank += (v.z > m || (v.z == m && 4 * q + 2 < lane)) ? 1 : 0;
+        rank += (v.w > m || (v.w == m && 4 * q + 3 < lane)) ? 1 : 0;
     }
-    const uint32_t T = __shfl_sync(kFull, m, __ffs(__ballot_sync(kFull, rank == K - 1)) - 1);
+    const uint32_t T = wm[__ffs(__ballot_sync(kFull, rank == K - 1)) - 1];
     int cnt = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) cnt += (16 * lane + j < E && k[j] >= T) ? 1 : 0;
-    int incl = cnt;
+    for (int j = 0; j < 16; ++j) cnt += (sel_id(lane, j) < E && k[j] >= T) ? 1 : 0;
+    // exclusive prefix and total of cnt (<= 16: five bits) from one ballot per bit
+    const unsigned lt = (1u << lane) - 1u;
+    int pre = 0, n = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += u;
+    for (int bit = 0; bit < 5; ++bit) {
+        const unsigned bb = __ballot_sync(kFull, (cnt >> bit) & 1);
+        pre += __popc(bb & lt) << bit;
+        n += __popc(bb) << bit;
     }
-    const int n = __shfl_sync(kFull, incl, 31);
     my_id = 0;
     my_val = 0.f;
     if (n <= 32) {
-        int at = incl - cnt;
+        int at = pre;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            if (16 * lane + j < E && k[j] >= T) {
-                ck[at] = k[j];
-                ci[at] = 16 * lane + j;
-                ++at;
-            }
+            if (sel_id(lane, j) < E && k[j] >= T) cand[at++] = make_uint2(k[j], (uint32_t)sel_id(lane, j));
         __syncwarp();
-        // lane c holds candidate c and ranks it against the others through shuffles
-        const uint32_t kc = lane < n ? ck[lane] : 0u;
-        const int ic = lane < n ? ci[lane] : 0x7fffffff;
+        // lane c ranks candidate c against all n (broadcast reads)
+        const uint2 me = lane < n ? cand[lane] : make_uint2(0u, 0x7fffffffu);
         int r = 0;
-#pragma unroll
-        for (int d = 0; d < 32; ++d) {
-            const uint32_t kd = __shfl_sync(kFull, kc, d);
-            const int id = __shfl_sync(kFull, ic, d);
-            r += (d < n && precedes(kd, id, kc, ic)) ? 1 : 0;
+        for (int d = 0; d < n; ++d) {
+            const uint2 o = cand[d];
+            r += precedes(o.x, (int)o.y, me.x, (int)me.y) ? 1 : 0;
         }
         if (lane < n && r < K) sel[r] = lane;
         __syncwarp();
         if (lane < K) {
-            const int c = sel[lane];
-            my_id = ci[c];
-            my_val = key_value(ck[c]);
+            const uint2 c = cand[sel[lane]];
+            my_id = (int)c.y;
+            my_val = key_value(c.x);
         }
         __syncwarp();
     } else {
-        warp_topk_by<16>([&](int e) { return e < E ? keys_t[(e & 15) * 32 + (e >> 4)] : 0u; }, K, my_id, my_val);
-    }
-}
-
-// RMSNorm scale of x (H = NV * 128 values) read through L2 (x written by other CTAs of the
-// same launch), every load issued before the arithmetic: the arithmetic and order of
-// rms_scale_warp exactly, so every path normalises identically.
-template <int NV>
-__device__ __forceinline__ float rms_scale_warp_cg(const float *x, float eps) {
-    const int lane = threadIdx.x & 31;
-    float4 v[NV];
+        unsigned left = 0u;  // bit j: candidate j of this lane is an expert not yet taken
 #pragma unroll
-    for (int m = 0; m < NV; ++m) v[m] = __ldcg(reinterpret_cast<const float4 *>(x + lane * 4 + 128 * m));
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int j = 0; j < 16; ++j) left |= (sel_id(lane, j) < E ? 1u : 0u) << j;
+        for (int r = 0; r < K; ++r) {
+            // this lane's first candidate in (key descending, index ascending) order
+            uint32_t bk = 0u;
+            int bi = 0x7fffffff;
 #pragma unroll
-    for (int m = 0; m < NV; ++m) {
-        a0 = fmaf(v[m].x, v[m].x, a0); a1 = fmaf(v[m].y, v[m].y, a1); a2 = fmaf(v[m].z, v[m].z, a2); a3 = fmaf(v[m].w, v[m].w, a3);
+            for (int j = 0; j < 16; ++j)
+                if (((left >> j) & 1u) && precedes(k[j], sel_id(lane, j), bk, bi)) { bk = k[j]; bi = sel_id(lane, j); }
+            // the warp's first: a strict total order, so every lane ends with the same winner
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const uint32_t ok = __shfl_xor_sync(kFull, bk, o);
+                const int oi = __shfl_xor_sync(kFull, bi, o);
+                if (precedes(ok, oi, bk, bi)) { bk = ok; bi = oi; }
+            }
+            if (lane == r) { my_id = bi; my_val = key_value(bk); }
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (sel_id(lane, j) == bi) left &= ~(1u << j);
+        }
+        __syncwarp();
     }
-    float ss = warp_sum((a0 + a1) + (a2 + a3));
-    return 1.0f / sqrtf(ss / (float)(NV * 128) + eps);
 }
 
 }  // namespace rl

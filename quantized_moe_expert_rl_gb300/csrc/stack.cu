@@ -49,6 +49,7 @@ static rl_status stack_entry(const rl_moe_shape *shp, int32_t layer0, int32_t n_
     a.x_hist = x_hist;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     a.ctr = reinterpret_cast<unsigned long long *>(w8);
+    a.ss = reinterpret_cast<long long *>(w8 + 128);
     const size_t accb = align_up(2 * (size_t)shp->n_experts * sizeof(long long), 256);
     a.acc = reinterpret_cast<long long *>(w8 + 256);
     a.acc_pg = reinterpret_cast<long long *>(w8 + 256 + accb);

@@ -61,14 +61,13 @@ constexpr uint32_t kSpinCap = 1u << 22;       // global-memory polls (~1 us each
 // router-column copy brings (its own wait on that copy runs out, the others then wait in vain
 // at the next grid barrier).
 constexpr int kStKnobWord = 16;  // u32 index of the knobs in the workspace header
-constexpr int kStSelWarps = 16;               // selection warps: E <= 32 * 16, one expert per thread
 constexpr int kStHdr = 1024;                  // barriers, scalars, CTA constants, outputs of the selection
 constexpr int kStPredMax = 32;                // experts prefetched on the pre-gated prediction
 constexpr int kStCand = 16;                   // single-warp selection: candidates per lane (E <= 512)
-// selection scratch: the 512 keys (transposed for warp_topk_thr), per warp 32 candidate keys,
-// 32 candidate ids and kMaxK results, then the layer's residency row (u64, copied ahead)
-constexpr int kStSelWarpBytes = (32 + 32 + kMaxK) * 4;
-constexpr int kStSelTab = 512 * 4 + kStWarps * kStSelWarpBytes;
+// selection scratch: the producer warp's 32 lane maxima, 32 (key, id) candidates and kMaxK
+// results, the layer's 512 keys, then its residency row (u64, copied ahead)
+constexpr int kStSelKeys = 128 + 256 + 4 * kMaxK;  // then the 512 keys of the layer
+constexpr int kStSelTab = kStSelKeys + 512 * 4;
 constexpr int kStSelBytes = kStSelTab + 512 * 8;
 static_assert(kStSelTab % 16 == 0, "the residency row copy needs a 16-byte aligned destination");
 // The warp that issues every bulk copy.  A memory fence waits for the bulk copies its own
@@ -93,7 +92,7 @@ __host__ __device__ inline int rc_rows(int E) { return (E + rc_nbox(E) - 1) / rc
 
 struct StLayout {
     int rmax, dmax, rowb, dtileb;
-    size_t rbs, rcb, o_x, o_xt, o_rc, o_xq, o_part, o_gu, o_dn, o_o, o_h, o_sel, total;
+    size_t rbs, rcb, o_xt, o_rc, o_xq, o_part, o_gu, o_dn, o_o, o_h, o_sel, total;
     __host__ __device__ StLayout(int H, int E, int K, int I, int G, bool pg) {
         const int U = gu_unit(H), units = K * I / U;
         rmax = ((units + G - 1) / G) * U;
@@ -103,9 +102,8 @@ struct StLayout {
         rcb = (size_t)rc_nbox(E) * rbs;
         rowb = (int)matrix_bytes(1, H);
         dtileb = (int)align_up(matrix_bytes(dmax, I), 16);
-        o_x = kStHdr + kTabBytes;
-        o_xt = o_x + (size_t)H * sizeof(float);
-        o_rc = align_up(o_xt + (size_t)H * sizeof(float), 128);  // x again, lane-transposed for the gate/up lanes
+        o_xt = kStHdr + kTabBytes;                               // x, lane-transposed for the gate/up lanes
+        o_rc = align_up(o_xt + (size_t)H * sizeof(float), 128);
         // router columns [q0, q0 + dmax) of every row of one layer (and of the next, pre-gating)
         o_xq = o_rc + (pg ? 2 : 1) * rcb;
         o_part = o_xq + align_up((size_t)dmax * sizeof(float), 16);  // this CTA's slice of x
@@ -124,7 +122,7 @@ struct StCta {
     int p0, p1, ka, kb, n0, n1;  // gate/up (expert, row) pairs: two segments (experts ka, kb)
     int q0, nq;                  // down output rows = this CTA's slice of x
     int rowb, dtileb, dmax, rbs, rcb;
-    uint32_t o_x, o_xt, o_rc, o_xq, o_part, o_gu, o_dn, o_o, o_h, o_sel;
+    uint32_t o_xt, o_rc, o_xq, o_part, o_gu, o_dn, o_o, o_h, o_sel;
 };
 
 struct StackArgs {
@@ -145,6 +143,7 @@ struct StackArgs {
     unsigned long long *ctr;
     long long *acc;     // [2][E] fixed-point router sums, by layer parity
     long long *acc_pg;  // [2][E] the same for the pre-gate dots (next layer's router, this input)
+    long long *ss;      // [2] sums of squares of x (rms_scale_warp's fixed point), by layer parity
     float *h;           // [K][I]
     uint32_t *pg_hits;  // [L] or NULL
     uint64_t *table_w;         // the table again, written by device fills (NULL without fill tables)
@@ -168,9 +167,9 @@ __device__ __forceinline__ void red_fixed(long long *dst, float p, int32_t *ctrl
         dev_error(ctrl, RL_DEVERR_RANGE);
         p = 0.f;
     }
-    atomicAdd(reinterpret_cast<unsigned long long *>(dst), (unsigned long long)__float2ll_rn(p * kFixScale));
+    atomicAdd(reinterpret_cast<unsigned long long *>(dst), (unsigned long long)float_to_ll(p * kFixScale));
 }
-__device__ __forceinline__ float fixed_value(long long v) { return __ll2float_rn(v) * kFixInv; }
+__device__ __forceinline__ float fixed_value(long long v) { return ll_to_float(v) * kFixInv; }
 
 // All CTAs of the grid meet; writes before it (through L2) are visible after it.  Thread 0
 // keeps the barrier target in a register; `target` = 0 means "not yet based".  The arrival is a
@@ -254,7 +253,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         C.dmax = lay.dmax;
         C.rbs = (int)lay.rbs;
         C.rcb = (int)lay.rcb;
-        C.o_x = (uint32_t)lay.o_x; C.o_xt = (uint32_t)lay.o_xt; C.o_rc = (uint32_t)lay.o_rc; C.o_xq = (uint32_t)lay.o_xq;
+        C.o_xt = (uint32_t)lay.o_xt; C.o_rc = (uint32_t)lay.o_rc; C.o_xq = (uint32_t)lay.o_xq;
         C.o_part = (uint32_t)lay.o_part; C.o_gu = (uint32_t)lay.o_gu; C.o_dn = (uint32_t)lay.o_dn;
         C.o_o = (uint32_t)lay.o_o; C.o_h = (uint32_t)lay.o_h; C.o_sel = (uint32_t)lay.o_sel;
         for (int i = 0; i < kStBars; ++i) mbar_init(&bars[i], 1);
@@ -333,6 +332,18 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     // fixed order per row) spreads them.
     auto add_partials = [&](int i) {
         const int nq = C.nq;
+        if (warp * 32 < nq) {
+            // the sum of squares of the slice, in rms_scale_warp's groups of 8 (the slice starts
+            // on a multiple of 8): one fixed-point partial per warp into ss[i & 1]
+            const float *xs = reinterpret_cast<const float *>(smem + C.o_xq);
+            const int t = threadIdx.x;
+            const float sg = sq8_lanes(t < nq ? xs[t] : 0.f);
+            bool rg = false;
+            long long v = ((t & 7) == 0 && t < nq) ? sq_fixed(sg, rg) : 0ll;
+            v = warp_sum_ll(v);
+            if (__any_sync(kFull, rg) && lane == 0) dev_error(a.ctrl, RL_DEVERR_RANGE);
+            if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long *>(a.ss + (i & 1)), (unsigned long long)v);
+        }
         if (me < E && nq > 0) {
             const float4 *xq = reinterpret_cast<const float4 *>(smem + C.o_xq);
             const int rows = rc_rows(E);
@@ -374,11 +385,13 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         if (threadIdx.x == kColThread) issue_tab(0);
         tab_pend = 0;
     }
-    if (blockIdx.x == 0)
+    if (blockIdx.x == 0) {
         for (int j = threadIdx.x; j < 2 * E; j += kStThreads) {
             __stcg(a.acc + j, 0ll);
             __stcg(a.acc_pg + j, 0ll);
         }
+        if (threadIdx.x < 2) __stcg(a.ss + threadIdx.x, 0ll);
+    }
     if ((int)threadIdx.x < C.nq) reinterpret_cast<float *>(smem + C.o_xq)[threadIdx.x] = __ldcg(a.x + C.q0 + threadIdx.x);
     if (hold == (int)blockIdx.x + 1) failed = true;  // test knob: this CTA never arrives
     if (!failed && !grid_sync(a.ctr, target, ok_s, a.ctrl, cap_grid)) failed = true;
@@ -396,56 +409,60 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         const int l = a.layer0 + i;
         const bool last = i + 1 == a.nl;
         ex_issued = false;
-        // ---------------- B: the logits, the selection (every warp on its own), x_l ----------------
-        // All threads read their logit accumulator while warp 0 forms the RMSNorm scale of x_l
-        // straight from L2; one CTA barrier, then the keys; one more, then every warp selects
-        // the top-k by itself, so the producer warp issues the expert copies from its own
-        // selection while the others stage x_l for the gate/up lanes.
-        const long long accv = me < E ? __ldcg(a.acc + (size_t)(i & 1) * E + me) : 0ll;
-        // this thread's share of x_l, loaded now and staged after the selection
+        // ---------------- B: the logits and the selection (the producer warp), x_l ----------------
+        // Every thread reads its expert's logit accumulator (coalesced), the layer's sum of
+        // squares and its share of x_l, forms its key and writes it to shared memory; after one
+        // CTA barrier the producer warp selects the top-k from the keys, looks the experts up,
+        // issues the expert copies, then records the selection and (CTA 0) writes the outputs,
+        // the miss count and the flag.  The other warps stage x_l for the gate/up lanes
+        // meanwhile; a second CTA barrier ends the phase.
         constexpr int kXv = (H / 4 + kStThreads - 1) / kStThreads;
-        float4 xv_r[kXv];
+        float4 xv_r[kXv];  // this thread's share of x_l, staged below
+        const long long accv = me < E ? __ldcg(a.acc + (size_t)(i & 1) * E + me) : 0ll;
+        const float biasv = (a.bias && me < E) ? __ldcg(a.bias + (size_t)l * E + me) : 0.f;
+        const long long ssv = __ldcg(a.ss + (i & 1));
 #pragma unroll
         for (int u = 0; u < kXv; ++u) {
             const int j = threadIdx.x + u * kStThreads;
             xv_r[u] = j < H / 4 ? __ldcg(reinterpret_cast<const float4 *>(a.x) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        if (warp == 0) {
-            const float r = a.eps >= 0.f ? rms_scale_warp_cg<NV>(a.x, a.eps) : 1.f;
-            if (lane == 0) *scale_s = r;
-        }
         // acc_pg[(i + 1) & 1] was last read in D of the previous layer; it takes this
         // layer's pre-gate sums next
         if (pregate && i > 0 && blockIdx.x == 0)
             for (int j = threadIdx.x; j < E; j += kStThreads) __stcg(a.acc_pg + (size_t)((i + 1) & 1) * E + j, 0ll);
-        cta_sync();
-        uint32_t *keys_t = reinterpret_cast<uint32_t *>(smem + C.o_sel);
-        if (threadIdx.x < 512) {
+        uint32_t *keys_s = reinterpret_cast<uint32_t *>(smem + C.o_sel + kStSelKeys);
+        {
             // logit = rs * (W x) + bias: the RMSNorm scale applied to the summed dots
+            const float rs = a.eps >= 0.f ? rms_scale_from(ssv, H, a.eps) : 1.f;
             uint32_t key = 0u;
             if (me < E) {
-                const float lv = fmaf(fixed_value(accv), *scale_s, a.bias ? a.bias[(size_t)l * E + me] : 0.f);
+                const float lv = fmaf(fixed_value(accv), rs, biasv);
                 key = order_key(lv);
                 if (blockIdx.x == 0) {
                     if (lv != lv) dev_error(a.ctrl, RL_DEVERR_NAN);
                     if (a.logits_out) a.logits_out[(size_t)l * E + me] = lv;
                 }
             }
-            keys_t[(me & 15) * 32 + (me >> 4)] = key;
+            keys_s[me] = key;
+            if (threadIdx.x == 0) *scale_s = rs;
         }
         cta_sync();
-        // Warp 0 (outputs, miss count, flag) and the producer warp (expert copies) select, each
-        // on its own: the same code on the same keys gives the same selection and decisions.
-        // The other warps stage x_l meanwhile.
         bool early = false;  // the producer warp issued the gate/up copies from its own selection
-        if (warp == 0 || warp == kStProducer) {
+        if (warp == kStProducer) {
             const int K = a.K;
+            uint32_t kk[16];  // in sel_id's layout: conflict-free 8-byte reads
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint2 v = reinterpret_cast<const uint2 *>(keys_s)[32 * c + lane];
+                kk[2 * c] = v.x;
+                kk[2 * c + 1] = v.y;
+            }
             int my_id;
             float my_val;
             {
-                uint8_t *ws = smem + C.o_sel + 2048 + warp * kStSelWarpBytes;
-                warp_topk_thr(keys_t, E, K, reinterpret_cast<uint32_t *>(ws), reinterpret_cast<int *>(ws + 128),
-                              reinterpret_cast<int *>(ws + 256), my_id, my_val);
+                uint8_t *ws = smem + C.o_sel;
+                warp_topk_thr(kk, E, K, reinterpret_cast<uint32_t *>(ws), reinterpret_cast<uint2 *>(ws + 128),
+                              reinterpret_cast<int *>(ws + 384), my_id, my_val);
             }
             uint64_t slot = 0;
             if (tab_smem) {
@@ -454,7 +471,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             } else if (lane < K) {
                 slot = __ldcg(a.table + (size_t)l * E + my_id);
             }
-            // both warps take the same decisions from the same selection
+            __syncwarp();
+            // the decisions of every CTA follow from the same selection
             const unsigned mmask = __ballot_sync(kFull, lane < K && slot == 0);
             const int nmiss = __popc(mmask);
             const bool bad = __ballot_sync(kFull, lane < K && slot != 0 && (slot & 15)) != 0;
@@ -468,11 +486,11 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 fillable = __all_sync(kFull, ok);
             }
             const bool stop = (nmiss > 0 && !fillable) || bad || flag0 <= l || failed;
-            if (warp == kStProducer && !stop && !(FILL && nmiss > 0)) {
+            if (!stop && !(FILL && nmiss > 0)) {
                 issue_gu(__shfl_sync(kFull, slot, C.ka), __shfl_sync(kFull, slot, C.kb));
                 early = true;
             }
-            if (warp == 0) {
+            {
                 if (lane < K) {
                     slots_s[lane] = slot;
                     sv_s[lane] = my_val;
@@ -506,23 +524,21 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             }
         }
         {
-            float *x_s = reinterpret_cast<float *>(smem + C.o_x);
+            // x_l lane-transposed for the gate/up lanes: float4 q of the slice of lane L of row
+            // half h (columns h H/SPLIT + L 8 GPL ...) sits at [h][q][L ^ q] (the xor spreads
+            // the staging writes of consecutive q over the banks)
             float4 *xt_s = reinterpret_cast<float4 *>(smem + C.o_xt);
-            // x_s in order; xt_s lane-transposed for the gate/up lanes: float4 q of the slice of
-            // lane L of row half h (columns h H/SPLIT + L 8 GPL ...) sits at [h][q][L ^ q] (the
-            // xor spreads the staging writes of consecutive q over the banks)
 #pragma unroll
             for (int u = 0; u < kXv; ++u) {
                 const int j = threadIdx.x + u * kStThreads;
                 if (j >= H / 4) break;
-                const float4 v = xv_r[u];
-                reinterpret_cast<float4 *>(x_s)[j] = v;
                 const int hf = H / 4 / SPLIT, h = j / hf, r = j % hf, L = r / (2 * GPL), q = r % (2 * GPL);
-                xt_s[(h * 2 * GPL + q) * 32 + (L ^ q)] = v;
+                xt_s[(h * 2 * GPL + q) * 32 + (L ^ q)] = xv_r[u];
             }
         }
         if (a.x_hist && blockIdx.x == 0)
-            for (int j = threadIdx.x; j < H; j += kStThreads) a.x_hist[(size_t)l * H + j] = __ldcg(a.x + j);
+            for (int j = threadIdx.x; j < H / 4; j += kStThreads)
+                reinterpret_cast<float4 *>(a.x_hist + (size_t)l * H)[j] = __ldcg(reinterpret_cast<const float4 *>(a.x) + j);
         tab_pend = -1;
         cta_sync();
         if (*stop_s) break;
@@ -659,8 +675,10 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
 
         // ---------------- D: down rows of every expert, ordered combine, residual ----------------
         // acc[i & 1] was read by every CTA in B; it takes the sums of layer index i + 2 next
-        if (blockIdx.x == 0)
+        if (blockIdx.x == 0) {
             for (int j = threadIdx.x; j < E; j += kStThreads) __stcg(a.acc + (size_t)(i & 1) * E + j, 0ll);
+            if (threadIdx.x == 0) __stcg(a.ss + (i & 1), 0ll);
+        }
         // the renormalised weights, needed first by the combine (off the path from the
         // selection to the expert copies); by a warp with the smaller share of the h staging
         if (warp == kStProducer - 1) {
@@ -758,11 +776,11 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         if ((int)threadIdx.x < C.nq) {
             const int r = C.q0 + threadIdx.x;
             const float *o_s = reinterpret_cast<const float *>(smem + C.o_o);
-            const float *x_s = reinterpret_cast<const float *>(smem + C.o_x);
+            float *xq = reinterpret_cast<float *>(smem + C.o_xq);  // this CTA's slice of x_l
             const float acc = ordered_combine(w_s, o_s + threadIdx.x, C.dmax, a.K);
-            const float xv = x_s[r] + acc;
+            const float xv = xq[threadIdx.x] + acc;
             __stcg(a.x + r, xv);
-            reinterpret_cast<float *>(smem + C.o_xq)[threadIdx.x] = xv;
+            xq[threadIdx.x] = xv;
         }
         if (last) break;
         // the next layer's router dots on this CTA's slice of x_{l+1}

@@ -466,14 +466,24 @@ def run_bounded_chunk(model: Model, b: PrefillBuffers, x: torch.Tensor, path: st
 
 
 def run_bounded_chunk_device(model: Model, b: PrefillBuffers, x: torch.Tensor, path: str = "tc",
-                             hist: dict | None = None) -> BoundedStats:
+                             hist: dict | None = None, timing: dict | None = None) -> BoundedStats:
     """Prefill chunk through model.L stacked layers with bounded residency and every fill done
     by the device: per layer rl_route (exact miss count, early-out flag), rl_fill_missing (the
     layer's absent selected experts copied from the pinned backing store into their slots, the
     slots re-resolved, the flag cleared), then the layer's experts, all enqueued at once with
     one host sync at the end.  Same selections, fills and outputs as run_bounded_chunk; the
-    early-out layers are the layers that missed.  hist as for run_bounded_chunk."""
+    early-out layers are the layers that missed.  hist as for run_bounded_chunk.
+    timing (optional, a dict): filled with the device time in ms of the three stages summed
+    over the layers ("route": RMSNorm + rl_route, "fill": rl_fill_missing, "experts": pair
+    build + grouped expert GEMMs), from CUDA events recorded on the current stream."""
     hist = hist or {}
+    ev = [] if timing is not None else None
+
+    def mark():
+        if ev is not None:
+            e = torch.cuda.Event(enable_timing=True)
+            e.record()
+            ev.append(e)
     T, shp = x.shape[0], model.shape
     src, dst = model.device_fill_tables()
     table0 = model.table_host.copy()
@@ -486,14 +496,28 @@ def run_bounded_chunk_device(model: Model, b: PrefillBuffers, x: torch.Tensor, p
     for l in range(model.L):
         if "x" in hist:
             hist["x"][l].copy_(x)
+        mark()
         enqueue_prefill_route(model, b, l, x, True, keep_logits="logits" in hist)
+        mark()
         for key, src_t in (("logits", b.logits), ("ids", b.ids), ("weights", b.weights), ("slots", b.slots)):
             if key in hist:
                 hist[key][l].copy_(src_t)
+        mark()
         L.rl_fill_missing(shp, l, T, b.ids, b.slots, model.table, src, dst, filled, first, b.ctrl, b.fill_ws,
                           b.fill_ws.numel())
+        mark()
         enqueue_prefill_experts(model, b, l, x, x, True, path)
+        mark()
     ctrl = b.ctrl.cpu()
+    if ev is not None:
+        torch.cuda.synchronize(model.device)
+        t = {"route": 0.0, "fill": 0.0, "experts": 0.0}
+        for l in range(model.L):
+            e = ev[5 * l:5 * l + 5]
+            t["route"] += e[0].elapsed_time(e[1])
+            t["fill"] += e[2].elapsed_time(e[3])
+            t["experts"] += e[3].elapsed_time(e[4])
+        timing.update(t)
     if int(ctrl[1]) != 0:
         raise RuntimeError(f"device error bits {int(ctrl[1])} in a device-filled chunk")
     model.sync_residency_from_device()

@@ -454,3 +454,77 @@ def test_decode_stack_device_fill():
     assert np.array_equal(m_d.resident, m_h.resident)
     assert int(filled.item()) == n_host_fills > 0
     print(f"device fills inside the fused launch: {n_host_fills} experts over {base.tokens} tokens, no stop")
+
+
+def test_decode_stack_bounded_full_shape(stack_model):
+    """Bounded residency at the full decode-stack shape: 48 layers x 512 experts with 435 of
+    them resident per layer (seeded), three tokens in turn from that residency, through the
+    stop / fill / resume flow and through the fills done inside the fused launch.  Both give
+    the bits of the fully resident model; the per-layer miss counts, the stopping layers and
+    the filled experts follow exactly from the fully resident run's selections and the
+    residency so far; sampled layers of the first token match the oracle from their own
+    inputs."""
+    engine = _engine()
+    w, m_full, _ = stack_model
+    wb = replace(w, n_resident=435)
+    m_b = engine.Model(wb)
+    ob = OracleSide(m_b)    # the bounded model's slot addresses point into its own pool
+    b_full, b_b = engine.DecodeBuffers.make(m_full), engine.DecodeBuffers.make(m_b)
+    toks = [0, 1, 2]
+    x = torch.from_numpy(synth.tokens(w, 0, 3)).cuda()
+    seeded = np.stack([synth.resident_mask(wb, l).astype(bool) for l in range(wb.n_layers)])
+    summary = {}
+    for mode in ("host", "device"):
+        m_b.reset_residency()
+        resident = seeded.copy()
+        filled = torch.zeros(1, dtype=torch.int32, device="cuda")
+        n_stop = n_fill = 0
+        for i, t in enumerate(toks):
+            y_full = torch.zeros(w.hidden, device="cuda")
+            y_b = torch.zeros(w.hidden, device="cuda")
+            hist = torch.zeros((m_b.L, w.hidden), device="cuda")
+            engine.enqueue_decode_token_fused(m_full, b_full, x[i], y_full)
+            b_b.miss.zero_()
+            if mode == "host":
+                st = engine.run_bounded_decode_token(m_b, b_b, x[i], y_b, x_hist=hist)
+            else:
+                engine.run_bounded_decode_token_device(m_b, b_b, x[i], y_b, filled, x_hist=hist)
+            torch.cuda.synchronize()
+            assert b_b.ctrl.tolist() == [0x7FFFFFFF, 0], (mode, t)
+            assert torch.equal(_bits(y_full), _bits(y_b)), (mode, t)
+            assert torch.equal(_bits(b_full.ids), _bits(b_b.ids)), (mode, t)
+            assert torch.equal(_bits(b_full.weights), _bits(b_b.weights)), (mode, t)
+            ids = b_full.ids.cpu().numpy()
+            exp_miss, exp_stop, exp_fill = [], [], []
+            for l in range(wb.n_layers):
+                miss = [int(e) for e in ids[l] if not resident[l, e]]
+                exp_miss.append(len(miss))
+                if miss:
+                    exp_stop.append(l)
+                    exp_fill += [(l, e) for e in sorted(set(miss))]
+                    resident[l, sorted(set(miss))] = True
+            assert b_b.miss.tolist() == exp_miss, (mode, t)
+            if mode == "host":
+                assert st.early_outs == exp_stop and st.filled == exp_fill, (mode, t)
+                n_stop += len(st.early_outs)
+            n_fill += len(exp_fill)
+            if i == 0:
+                # sampled layers of the first token against the oracle from their own inputs
+                H = hist.double().cpu().numpy()
+                y_last = y_b.double().cpu().numpy()
+                sl = u64(b_b.slots)
+                wts = b_b.weights.cpu().numpy()
+                for l in (0, 17, wb.n_layers - 1):
+                    xn = oracle.rmsnorm(H[l:l + 1])
+                    y_o = oracle.moe_experts(xn, ids[l:l + 1], wts[l:l + 1].astype(np.float64), sl[l:l + 1],
+                                             ob.record, w.hidden, w.inter, ob.grid)
+                    x_next = H[l + 1] if l + 1 < wb.n_layers else y_last
+                    assert rel_l2(x_next - H[l], y_o[0]) <= REL_F32, (mode, l)
+        if mode == "device":
+            assert int(filled.item()) == n_fill
+            m_b.sync_residency_from_device()
+        assert np.array_equal(m_b.resident, resident), mode
+        summary[mode] = (n_stop, n_fill)
+    print(f"bounded full-shape decode: {summary['host'][0]} stops and {summary['host'][1]} fills over "
+          f"{len(toks)} tokens; device fills {summary['device'][1]}, no stop")
+    assert summary["host"][1] == summary["device"][1] > 0

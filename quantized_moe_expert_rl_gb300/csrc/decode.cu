@@ -129,13 +129,13 @@ __global__ void __launch_bounds__(kGuThreads) dec_gateup_kernel(const float *__r
     constexpr int kTeams = kGuThreads / 32 / SPLIT;
     // lane's 8*GPL consecutive inputs: columns half*H/SPLIT + lane*8*GPL ...
     const int c0 = half * (H / SPLIT) + lane * 8 * GPL;
-    float xv[8 * GPL];
+    unsigned long long xv[4 * GPL];  // the lane's inputs as packed f32 pairs
     {
         const float r = NORM ? *scale_s : 1.f;
 #pragma unroll
         for (int q = 0; q < 2 * GPL; ++q) {
             const float4 v = reinterpret_cast<const float4 *>(x_s + c0)[q];
-            xv[4 * q] = v.x * r; xv[4 * q + 1] = v.y * r; xv[4 * q + 2] = v.z * r; xv[4 * q + 3] = v.w * r;
+            pack4(make_float4(v.x * r, v.y * r, v.z * r, v.w * r), &xv[2 * q]);
         }
     }
     const uint4 *tabc = tab + (lane & (kTabCopies - 1));
@@ -235,12 +235,10 @@ __global__ void dec_down_kernel(const uint64_t *__restrict__ slots, const float 
     constexpr int kRowsPerPass = 32 / LPR;
     uint64_t sk = 0;
     if (threadIdx.x < K) sk = __ldcg(slots + threadIdx.x);
-    float hv[8 * GPL];
+    unsigned long long hv[4 * GPL];  // h of the warp's expert as packed f32 pairs
 #pragma unroll
-    for (int q = 0; q < 2 * GPL; ++q) {
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(h + (size_t)k * I + sl * 8 * GPL) + q);
-        hv[4 * q] = v.x; hv[4 * q + 1] = v.y; hv[4 * q + 2] = v.z; hv[4 * q + 3] = v.w;
-    }
+    for (int q = 0; q < 2 * GPL; ++q)
+        pack4(__ldcg(reinterpret_cast<const float4 *>(h + (size_t)k * I + sl * 8 * GPL) + q), &hv[2 * q]);
     if (flag <= layer) return;
     const bool bad = threadIdx.x < K && (sk == 0 || (sk & 15));
     if (bad) dev_error(ctrl, sk == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN);

@@ -15,18 +15,19 @@ __host__ __device__ inline int gu_unit(int H) { return H >= 2048 ? 1 : 2048 / H;
 // warps per row: wide rows are split in two halves so that a lane holds only 32 inputs
 __host__ __device__ inline int gu_split(int H) { return H >= 1024 ? 2 : 1; }
 
-// Partial (gate, up) dots of one lane for one row pair.
+// Partial (gate, up) dots of one lane for one row pair; xp = the lane's 8 GPL inputs as packed
+// f32 pairs.
 template <int GPL>
-__device__ __forceinline__ void gu_row(const uint8_t *gb, const uint8_t *ub, int g0, const float *xv,
+__device__ __forceinline__ void gu_row(const uint8_t *gb, const uint8_t *ub, int g0, const unsigned long long *xp,
                                        const uint4 *tabc, float &gv, float &uv) {
-    float ge = 0.f, go = 0.f, ue = 0.f, uo = 0.f;
+    unsigned long long ga = 0ull, ua = 0ull;
 #pragma unroll
     for (int g = 0; g < GPL; ++g) {
-        group_fma_s(*reinterpret_cast<const uint16_t *>(gb + 2 + 2 * (g0 + g)), &xv[8 * g], tabc, ge, go);
-        group_fma_s(*reinterpret_cast<const uint16_t *>(ub + 2 + 2 * (g0 + g)), &xv[8 * g], tabc, ue, uo);
+        ga = group_fma2(*reinterpret_cast<const uint16_t *>(gb + 2 + 2 * (g0 + g)), &xp[4 * g], tabc, ga);
+        ua = group_fma2(*reinterpret_cast<const uint16_t *>(ub + 2 + 2 * (g0 + g)), &xp[4 * g], tabc, ua);
     }
-    gv = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(gb)) * (ge + go);
-    uv = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(ub)) * (ue + uo);
+    gv = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(gb)) * hsum2(ga);
+    uv = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(ub)) * hsum2(ua);
 }
 
 // h = silu(g) * u from the per-half partial sums of one row pair ([half][gate, up])
@@ -38,20 +39,20 @@ __device__ __forceinline__ float swiglu_part(const float *p) {
 }
 
 // One row of a down tile (rows of I values stored back to back from a block boundary), LPR
-// lanes per row, GPL groups per lane; hv = the lane's 8*GPL values of h.  Every lane of the
-// LPR-group returns the full dot product.
+// lanes per row, GPL groups per lane; hp = the lane's 8*GPL values of h as packed f32 pairs.
+// Every lane of the LPR-group returns the full dot product.
 template <int GPL, int LPR>
-__device__ __forceinline__ float down_row(const uint8_t *tile, int rr, int I, int sl, const float *hv,
+__device__ __forceinline__ float down_row(const uint8_t *tile, int rr, int I, int sl, const unsigned long long *hp,
                                           const uint4 *tabc) {
     const int gtile = rr * (I / 8) + sl * GPL;  // group index inside the tile
     const uint8_t *blk = tile + (gtile >> 5) * kBlockBytes;
     const int g0 = gtile & 31;
-    float ae = 0.f, ao = 0.f;
+    unsigned long long acc = 0ull;
 #pragma unroll
     for (int g = 0; g < GPL; ++g)
-        group_fma_s(*reinterpret_cast<const uint16_t *>(blk + 2 + 2 * (g0 + g)), &hv[8 * g], tabc, ae, ao);
+        acc = group_fma2(*reinterpret_cast<const uint16_t *>(blk + 2 + 2 * (g0 + g)), &hp[4 * g], tabc, acc);
     const float d = fp16_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
-    return group_sum<LPR>(d * (ae + ao));
+    return group_sum<LPR>(d * hsum2(acc));
 }
 
 // sum_k w_k * o_k in selection order (o_k at o[k * stride])

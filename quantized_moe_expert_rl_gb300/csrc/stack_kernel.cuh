@@ -584,14 +584,14 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             const int half = warp % SPLIT, team = warp / SPLIT;
             constexpr int kTeams = kStWarps / SPLIT;
             const int c0 = half * (H / SPLIT) + lane * 8 * GPL;
-            float xv[8 * GPL];
+            unsigned long long xv[4 * GPL];  // the lane's inputs as packed f32 pairs
             {
                 const float r = *scale_s;
                 const float4 *xt_s = reinterpret_cast<const float4 *>(smem + C.o_xt);
 #pragma unroll
                 for (int q = 0; q < 2 * GPL; ++q) {
                     const float4 v = xt_s[(half * 2 * GPL + q) * 32 + (lane ^ q)];
-                    xv[4 * q] = v.x * r; xv[4 * q + 1] = v.y * r; xv[4 * q + 2] = v.z * r; xv[4 * q + 3] = v.w * r;
+                    pack4(make_float4(v.x * r, v.y * r, v.z * r, v.w * r), &xv[2 * q]);
                 }
             }
             const uint4 *tabc = tab + (lane & (kTabCopies - 1));
@@ -746,13 +746,10 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 const int mine = jg < nq ? (nq - jg + ngk - 1) / ngk : 0;
                 const int trips = (int)__reduce_max_sync(kFull, (unsigned)mine);
                 const int I = a.I, dmax = C.dmax;
-                float hv[8 * DGPL];
+                unsigned long long hv[4 * DGPL];  // h of the lane's expert as packed f32 pairs
                 const float4 *h_s = reinterpret_cast<const float4 *>(smem + C.o_h) + (size_t)k * (I / 4);
 #pragma unroll
-                for (int q = 0; q < 2 * DGPL; ++q) {
-                    const float4 v = h_s[q * LPR + (sl ^ q)];
-                    hv[4 * q] = v.x; hv[4 * q + 1] = v.y; hv[4 * q + 2] = v.z; hv[4 * q + 3] = v.w;
-                }
+                for (int q = 0; q < 2 * DGPL; ++q) pack4(h_s[q * LPR + (sl ^ q)], &hv[2 * q]);
                 if (trips > 0 && !mbar_wait_warp(bar_dn, ph, cap_wait)) {
                     failed = true;
                 } else {

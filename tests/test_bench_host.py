@@ -50,9 +50,12 @@ def test_recorded_traffic_is_per_launch():
         # reported while the sources match the capture, else null (never a stale figure)
         want = float(e["dram_bytes_per_unit"]) if e["src_digest"] == bench._src_digest(k) else None
         assert bench._traffic(k, 1.0) == want
-    # the decode stack moves its algorithmic bytes and little more (no re-reads)
+    # the decode stack reads its algorithmic bytes and little more (no re-reads); the writes
+    # of a capture include dirty L2 lines that earlier launches left behind
     alg = 48 * (10 * 811008 + 512 * 2048 * 4 + 2 * 2048 * 4)
-    assert 1.0 <= d["moe_decode_stack"]["dram_bytes_per_unit"] / alg < 1.01
+    e = d["moe_decode_stack"]
+    assert 1.0 <= e["dram_bytes_read_per_unit"] / alg < 1.01
+    assert e["dram_bytes_read_per_unit"] <= e["dram_bytes_per_unit"] < 1.02 * alg
 
 
 def test_clock_summary_reads_reasons_and_median():

@@ -523,9 +523,39 @@ def decode_layer_leg(dev, steps: int, warmup: int) -> dict:
     roof = moe_decode_roofline(model, b, x, False, 16, stream, dev)
     ctrl = b.ctrl.cpu().tolist()
     assert ctrl == [0x7FFFFFFF, 0], ctrl
+    # the same tokens through moe_decode_layer: router and experts of a token in one launch
+    bf = engine.DecodeBuffers.make(model)
+    yf = torch.zeros_like(x)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(T)]
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            for t in range(T):
+                engine.enqueue_decode_layer_fused(model, bf, x[t], yf[t])
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(steps):
+            for t in range(T):
+                engine.enqueue_decode_layer_fused(model, bf, x[t], yf[t])
+        f1.record(stream)
+        for t in range(T):                            # each launch alone, for the roofline
+            evs[t][0].record(stream)
+            engine.enqueue_decode_layer_fused(model, bf, x[t], yf[t])
+            evs[t][1].record(stream)
+    stream.synchronize()
+    assert bf.ctrl.cpu().tolist() == [0x7FFFFFFF, 0]
+    msf = f0.elapsed_time(f1) / steps
+    t_launch = sum(a_.elapsed_time(b_) for a_, b_ in evs) / T * 1e-3
+    bytes_launch = w.top_k * w.record_bytes + w.n_experts * w.hidden * 4 + 2 * w.hidden * 4
+    peak, peak_kind = _peaks()
+    froof = {"bound": "hbm", "achieved": bytes_launch / t_launch / 1e9, "peak": peak, "unit": "GB/s",
+             "frac": bytes_launch / t_launch / 1e9 / peak, "traffic": None,
+             "kernel": "moe_decode_layer (router + experts of one token, one launch)",
+             "bytes_per_launch": bytes_launch, "launch_us": t_launch * 1e6, "peak_source": f"{peak_kind} hbm_gbs"}
     return {"workload": "decode_layer (1 layer, 1000 tokens one at a time)",
-            "path": "per-token CUDA graph: rl_route + moe_decode (3 kernels)",
-            "tokens_per_s": T / (ms * 1e-3), "us_per_token": ms * 1e3 / T, "roofline": roof,
+            "path": "one moe_decode_layer launch per token (router + experts)",
+            "tokens_per_s": T / (msf * 1e-3), "us_per_token": msf * 1e3 / T, "roofline": froof,
+            "chain": {"path": "per-token CUDA graph: rl_route + moe_decode (3 kernels)",
+                      "tokens_per_s": T / (ms * 1e-3), "us_per_token": ms * 1e3 / T, "roofline": roof},
             "target": "expert GEMVs at >= 70% of HBM peak"}
 
 

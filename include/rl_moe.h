@@ -269,6 +269,25 @@ rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, int32_t n_la
                            uint32_t *pregate_hits, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_decode_layer - rl_route (T = 1) then moe_decode (accumulate = 0) of ONE token in ONE
+ * launch, without a residual: y = sum_{k in order} weights[layer][k] * down_k(silu(gate_k xn)
+ * * (up_k xn)) with xn = x (norm_eps < 0) or RMSNorm(x) (norm_eps >= 0).  It is the fused
+ * kernel of moe_decode_stack run for a single layer, with y written instead of the residual
+ * stream ("Red Lite dev21 - GPU-routed decode", "What changed": the router and the experts of
+ * a decode token with no host round trip between them).  The router logits are summed across
+ * CTAs in fixed point as in moe_decode_stack (they may differ from rl_route's in the last
+ * bits).  If the layer selects an absent expert, ids/weights/slots[layer] and miss[layer] are
+ * written, ctrl[0] = min(ctrl[0], layer) and y is not written, so the caller can fill,
+ * rl_resolve_slots and moe_decode.  Does nothing when ctrl[0] < layer.
+ * x [H] f32 (read only, 16-byte aligned); y [H] f32; the other arguments and ws as for
+ * moe_decode_stack (ws: moe_decode_stack_workspace_bytes, zero-filled before its first use).
+ */
+rl_status moe_decode_layer(const rl_moe_shape *shp, int32_t layer, const float *x, float norm_eps,
+                           const float *w_router, const float *bias, const uint64_t *residency,
+                           const int8_t *codebook, int32_t *ids, float *weights, uint64_t *slots, uint32_t *miss,
+                           int32_t *ctrl, float *logits_out, float *y, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * moe_decode_stack_fill - moe_decode_stack (no pre-gating) where a layer that selects absent
  * experts does not stop the launch: the device fills them ("Red Lite dev23", "What changed",
  * item 1: the layer's missing experts are loaded and it runs with the experts the router

@@ -24,7 +24,7 @@ EXPORTS = ("rl_abi_version", "rl_last_error", "rl_record_bytes", "rl_rmsnorm", "
            "rl_build_pairs_workspace_bytes", "rl_build_pairs", "moe_prefill_workspace_bytes",
            "moe_prefill_chunk", "moe_prefill_chunk_f32", "moe_decode_static", "moe_decode_stack_workspace_bytes",
            "moe_decode_stack", "rl_fill_workspace_bytes", "rl_fill_missing", "rl_host_device_pointer",
-           "moe_decode_stack_fill")
+           "moe_decode_stack_fill", "moe_decode_layer")
 
 
 class RlShape(ctypes.Structure):
@@ -77,6 +77,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_prefill_chunk_f32": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]),
         "moe_decode_stack_fill": (i32, [shp, i32, i32, vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                         vp, vp, sz, vp]),
+        "moe_decode_layer": (i32, [shp, i32, vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "rl_fill_workspace_bytes": (sz, [shp]),
         "rl_fill_missing": (i32, [shp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "rl_host_device_pointer": (i32, [vp, ctypes.POINTER(ctypes.c_uint64)]),
@@ -199,6 +200,14 @@ def moe_decode_stack_fill(shape, layer0, n_layers, x, norm_eps, w_router, bias, 
         ctypes.byref(shape), layer0, n_layers, ptr(x), float(norm_eps), ptr(w_router), ptr(bias), ptr(residency),
         ptr(codebook), ptr(ids), ptr(weights), ptr(slots), ptr(miss), ptr(ctrl), ptr(logits_out), ptr(x_hist),
         ptr(fill_src), ptr(fill_dst), ptr(filled), ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_decode_layer(shape, layer, x, norm_eps, w_router, bias, residency, codebook, ids, weights, slots, miss, ctrl,
+                     logits_out, y, ws, ws_bytes, stream=None):
+    _check("moe_decode_layer", load().moe_decode_layer(
+        ctypes.byref(shape), layer, ptr(x), float(norm_eps), ptr(w_router), ptr(bias), ptr(residency), ptr(codebook),
+        ptr(ids), ptr(weights), ptr(slots), ptr(miss), ptr(ctrl), ptr(logits_out), ptr(y), ptr(ws), ws_bytes,
+        _stream(stream)))
 
 
 def rl_build_pairs_workspace_bytes(shape, T) -> int:

@@ -1,6 +1,6 @@
-// stack.cu - the ABI entry points of the fused decode stack (moe_decode_stack,
-// moe_decode_stack_fill); the kernel itself is in stack_kernel.cuh, its device-fill variants
-// are instantiated in stack_fill.cu.
+// stack.cu - the ABI entry points of the fused decode kernel (moe_decode_stack,
+// moe_decode_stack_fill, moe_decode_layer); the kernel itself is in stack_kernel.cuh, its
+// device-fill variants are instantiated in stack_fill.cu.
 #include "stack_kernel.cuh"
 
 using namespace rl;
@@ -15,8 +15,8 @@ static rl_status stack_entry(const rl_moe_shape *shp, int32_t layer0, int32_t n_
                              const float *w_router, const float *bias, uint64_t *residency, const int8_t *codebook,
                              int32_t *ids, float *weights, uint64_t *slots, uint32_t *miss, int32_t *ctrl,
                              float *logits_out, float *x_hist, int32_t pregate, uint32_t *pregate_hits,
-                             const uint64_t *fill_src, const uint64_t *fill_dst, uint32_t *filled, void *ws,
-                             size_t ws_bytes, void *stream) {
+                             const uint64_t *fill_src, const uint64_t *fill_dst, uint32_t *filled, float *y,
+                             void *ws, size_t ws_bytes, void *stream) {
     rl_status st = check_shape(shp);
     if (st != RL_OK) return st;
     if (layer0 < 0 || n_layers < 0 || layer0 + n_layers > shp->n_layers)
@@ -60,6 +60,7 @@ static rl_status stack_entry(const rl_moe_shape *shp, int32_t layer0, int32_t n_
     a.fill_src = fill_src;
     a.fill_dst = fill_dst;
     a.filled = filled;
+    a.y = y;
     a.layer0 = layer0;
     a.nl = n_layers;
     a.n_layers = shp->n_layers;
@@ -80,7 +81,7 @@ extern "C" rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, i
     // without fill tables the residency table is only read
     return stack_entry(shp, layer0, n_layers, x, norm_eps, w_router, bias, const_cast<uint64_t *>(residency),
                        codebook, ids, weights, slots, miss, ctrl, logits_out, x_hist, pregate, pregate_hits, nullptr,
-                       nullptr, nullptr, ws, ws_bytes, stream);
+                       nullptr, nullptr, nullptr, ws, ws_bytes, stream);
 }
 
 extern "C" rl_status moe_decode_stack_fill(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x,
@@ -91,5 +92,18 @@ extern "C" rl_status moe_decode_stack_fill(const rl_moe_shape *shp, int32_t laye
                                            uint32_t *filled, void *ws, size_t ws_bytes, void *stream) {
     if (!fill_src || !fill_dst || !filled) return fail(RL_ERR_INVALID, "moe_decode_stack_fill: NULL fill argument");
     return stack_entry(shp, layer0, n_layers, x, norm_eps, w_router, bias, residency, codebook, ids, weights, slots,
-                       miss, ctrl, logits_out, x_hist, 0, nullptr, fill_src, fill_dst, filled, ws, ws_bytes, stream);
+                       miss, ctrl, logits_out, x_hist, 0, nullptr, fill_src, fill_dst, filled, nullptr, ws, ws_bytes,
+                       stream);
+}
+
+extern "C" rl_status moe_decode_layer(const rl_moe_shape *shp, int32_t layer, const float *x, float norm_eps,
+                                      const float *w_router, const float *bias, const uint64_t *residency,
+                                      const int8_t *codebook, int32_t *ids, float *weights, uint64_t *slots,
+                                      uint32_t *miss, int32_t *ctrl, float *logits_out, float *y, void *ws,
+                                      size_t ws_bytes, void *stream) {
+    if (!y) return fail(RL_ERR_INVALID, "moe_decode_layer: NULL y");
+    // x is only read in this mode (the kernel writes y instead of the residual stream)
+    return stack_entry(shp, layer, 1, const_cast<float *>(x), norm_eps, w_router, bias,
+                       const_cast<uint64_t *>(residency), codebook, ids, weights, slots, miss, ctrl, logits_out,
+                       nullptr, 0, nullptr, nullptr, nullptr, nullptr, y, ws, ws_bytes, stream);
 }

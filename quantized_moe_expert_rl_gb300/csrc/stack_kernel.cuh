@@ -150,6 +150,7 @@ struct StackArgs {
     const uint64_t *fill_src;  // [L][E] device-readable record sources, or NULL (stop on a miss instead)
     const uint64_t *fill_dst;  // [L][E] HBM slots
     uint32_t *filled;          // experts filled by the device
+    float *y;                  // one layer without residual: y = MoE(xn), x left unchanged (NULL: the stack)
     int layer0, nl, H, E, K, I, pregate, n_layers;
 };
 
@@ -775,9 +776,13 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             const float *o_s = reinterpret_cast<const float *>(smem + C.o_o);
             float *xq = reinterpret_cast<float *>(smem + C.o_xq);  // this CTA's slice of x_l
             const float acc = ordered_combine(w_s, o_s + threadIdx.x, C.dmax, a.K);
-            const float xv = xq[threadIdx.x] + acc;
-            __stcg(a.x + r, xv);
-            xq[threadIdx.x] = xv;
+            if (a.y) {
+                a.y[r] = acc;  // a single layer (nl = 1): the loop ends below
+            } else {
+                const float xv = xq[threadIdx.x] + acc;
+                __stcg(a.x + r, xv);
+                xq[threadIdx.x] = xv;
+            }
         }
         if (last) break;
         // the next layer's router dots on this CTA's slice of x_{l+1}

@@ -212,6 +212,16 @@ def enqueue_decode_token(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_o
     y_out.copy_(b.x)
 
 
+def enqueue_decode_layer_fused(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
+                               layer: int = 0, keep_logits: bool = False) -> None:
+    """One token through one layer without norm or residual, router and experts in ONE launch
+    (moe_decode_layer): y_out = MoE_layer(x_in), the same as enqueue_decode_token(stacked=False)
+    for a one-layer model up to the order of the router's sums."""
+    L.moe_decode_layer(model.shape, layer, x_in, -1.0, model.routers, model.bias, model.table, model.codebook,
+                       b.ids, b.weights, b.slots, b.miss, b.ctrl, b.logits if keep_logits else None, y_out,
+                       b.stack_ws, b.stack_ws.numel())
+
+
 def enqueue_decode_token_fused(model: Model, b: DecodeBuffers, x_in: torch.Tensor, y_out: torch.Tensor,
                                keep_logits: bool = False, x_hist: torch.Tensor | None = None,
                                layer0: int = 0, pregate: int = 0,

@@ -104,6 +104,26 @@ def test_decode_stack_host_checks(lib):
     assert lib.moe_decode_stack(ctypes.byref(s), 48, 0, *args, need, None) == RL_OK
 
 
+def test_decode_layer_host_checks(lib):
+    """moe_decode_layer: the checks made before any launch (NULL y, layer out of range,
+    workspace too small, misaligned x)."""
+    from quantized_moe_expert_rl_gb300._lib import RL_ERR_INVALID, RlShape
+    s = RlShape.of(2048, 512, 10, 512, 1)
+    need = lib.moe_decode_stack_workspace_bytes(ctypes.byref(s))
+    fake = ctypes.c_void_p(1 << 20)
+    # x, eps, router, bias, table, codebook, ids, weights, slots, miss, ctrl, logits, y
+    args = [fake, -1.0, fake, None, fake, fake, fake, fake, fake, fake, fake, None, fake]
+    bad = list(args)
+    bad[12] = None
+    assert lib.moe_decode_layer(ctypes.byref(s), 0, *bad, fake, need, None) == RL_ERR_INVALID
+    assert b"NULL y" in lib.rl_last_error()
+    assert lib.moe_decode_layer(ctypes.byref(s), 1, *args, fake, need, None) == RL_ERR_INVALID
+    assert lib.moe_decode_layer(ctypes.byref(s), 0, *args, fake, need - 256, None) == RL_ERR_INVALID
+    bad = list(args)
+    bad[0] = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.moe_decode_layer(ctypes.byref(s), 0, *bad, fake, need, None) == RL_ERR_INVALID
+
+
 def test_fill_host_checks(lib):
     """rl_fill_missing, moe_decode_stack_fill and rl_host_device_pointer: the checks made
     before any launch (no GPU needed)."""

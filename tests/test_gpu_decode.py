@@ -66,6 +66,52 @@ def test_decode_layer_sampled_tokens(layer_model):
     assert rep.get("near_ties", 0) == 0
 
 
+def test_decode_layer_fused(layer_model):
+    """moe_decode_layer (router and experts of one token in one launch, no norm, no residual)
+    on 200 of the 1000 single-layer tokens: routing bit-exact on the GPU's own logits, logits
+    within the fused kernel's bound of the row scale (fixed-point sums across CTAs), outputs
+    within the f32 bound of the oracle, and the ids of rl_route + moe_decode except at a
+    genuine near tie."""
+    engine = _engine()
+    w, m, o = layer_model
+    b, bc = engine.DecodeBuffers.make(m), engine.DecodeBuffers.make(m)
+    sample = np.unique(np.concatenate([np.arange(3, w.tokens, 5), [w.tokens - 1]]))
+    x = torch.from_numpy(synth.tokens(w, 0, w.tokens)).cuda()
+    n = len(sample)
+    y = torch.zeros((n, w.hidden), device="cuda")
+    yc = torch.zeros((n, w.hidden), device="cuda")
+    lg = torch.zeros((n, w.n_experts), device="cuda")
+    ids = torch.zeros((n, w.top_k), dtype=torch.int32, device="cuda")
+    idc = torch.zeros((n, w.top_k), dtype=torch.int32, device="cuda")
+    wts = torch.zeros((n, w.top_k), device="cuda")
+    sl = torch.zeros((n, w.top_k), dtype=torch.int64, device="cuda")
+    for i, t in enumerate(sample):
+        engine.enqueue_decode_layer_fused(m, b, x[t], y[i], keep_logits=True)
+        lg[i].copy_(b.logits[0])
+        ids[i].copy_(b.ids[0])
+        wts[i].copy_(b.weights[0])
+        sl[i].copy_(b.slots[0])
+        engine.enqueue_decode_token(m, bc, x[t], yc[i], stacked=False)
+        idc[i].copy_(bc.ids[0])
+    torch.cuda.synchronize()
+    assert b.ctrl.tolist() == [0x7FFFFFFF, 0] and int(b.miss[0]) == 0
+    xo = x[torch.from_numpy(sample).cuda()].double().cpu().numpy()
+    rep = {}
+    r = check_route(lg.cpu().numpy(), ids.cpu().numpy(), wts.cpu().numpy(), u64(sl),
+                    oracle.router_logits(xo, o.router(0)), o.table_row(0), w.top_k, 0, rep, logit_tol=LOGIT_FIXED)
+    y_o = o.experts(xo, r.ids, r.weights, r.slots)
+    yg = y.double().cpu().numpy()
+    errs = [rel_l2(yg[i], y_o[i]) for i in range(n)]
+    same = np.all(ids.cpu().numpy() == idc.cpu().numpy(), axis=1)
+    yd = yc.double().cpu().numpy()
+    for i in np.nonzero(same)[0]:
+        assert rel_l2(yg[i], yd[i]) <= REL_F32, i
+    print(f"decode_layer fused: {n} tokens, worst rel L2 {max(errs):.2e}, logit err {rep['logit_err']:.2e}, "
+          f"near ties {rep.get('near_ties', 0)}, ids as rl_route on {int(same.sum())}/{n}")
+    assert max(errs) <= REL_F32
+    assert rep.get("near_ties", 0) <= 1 and int(same.sum()) >= n - 1
+
+
 def test_decode_graph_equals_eager(layer_model):
     engine = _engine()
     w, m, _ = layer_model

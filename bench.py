@@ -577,13 +577,10 @@ def bounded_decode_leg(dev, n_tokens: int = 16) -> dict:
     b = engine.DecodeBuffers.make(model)
     x = torch.from_numpy(synth.tokens(w, 0, n_tokens)).to(dev)
     y = torch.zeros_like(x)
-    res = {}
-    for mode in ("device", "host"):
-        model.reset_residency()
-        filled = torch.zeros(1, dtype=torch.int32, device=dev)
+    pass_stats = {}
+
+    def one_pass(mode, filled):
         stops = fills = misses = 0
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
         for t in range(n_tokens):
             b.miss.zero_()
             if mode == "device":
@@ -593,10 +590,24 @@ def bounded_decode_leg(dev, n_tokens: int = 16) -> dict:
                 stops += len(st.early_outs)
                 fills += len(st.filled)
             misses += int(b.miss.sum().item())
+        pass_stats.update(stops=stops, fills=fills, misses=misses)
+
+    res = {}
+    for mode in ("device", "host"):
+        # one untimed pass over the same tokens first (first use of the mapped backing store,
+        # the fill tables, the code), then the timed pass from the seeded residency again
+        for timed in (False, True):
+            model.reset_residency()
+            filled = torch.zeros(1, dtype=torch.int32, device=dev)
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            one_pass(mode, filled)
+            if timed:
+                break
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
-        if mode == "device":
-            fills = int(filled.item())
+        fills = int(filled.item()) if mode == "device" else pass_stats["fills"]
+        stops, misses = pass_stats["stops"], pass_stats["misses"]
         assert b.ctrl.cpu().tolist() == [0x7FFFFFFF, 0]
         res[mode] = {"tokens_per_s": n_tokens / wall, "ms_per_token": wall * 1e3 / n_tokens,
                      "experts_filled": fills, "misses": misses}

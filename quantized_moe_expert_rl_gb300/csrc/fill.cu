@@ -52,9 +52,7 @@ __global__ void __launch_bounds__(256) fill_copy_kernel(const uint32_t *__restri
         const uint64_t s = src[e], d = dst[e];
         if (s == 0 || d == 0 || ((s | d) & 15)) continue;  // finalize reports it
         const uint32_t lo = (uint32_t)c * kFillChunk, hi = min(rec_bytes, lo + (uint32_t)kFillChunk);
-        const uint4 *sp = reinterpret_cast<const uint4 *>(s + lo);
-        uint4 *dp = reinterpret_cast<uint4 *>(d + lo);
-        for (uint32_t j = threadIdx.x; j < (hi - lo) / 16; j += blockDim.x) dp[j] = sp[j];
+        copy16_batched(reinterpret_cast<uint4 *>(d + lo), reinterpret_cast<const uint4 *>(s + lo), (hi - lo) / 16);
     }
 }
 

@@ -115,6 +115,25 @@ __device__ __forceinline__ long long float_to_ll(float f) {
     return (long long)hi * 16777216ll + lo;
 }
 
+// dst[j] = src[j] for j < n (16-byte items) by the whole block, four loads in flight per
+// thread before their stores: a source across the host link takes microseconds per load, so
+// one load at a time per thread leaves the link mostly idle.
+__device__ __forceinline__ void copy16_batched(uint4 *__restrict__ dst, const uint4 *__restrict__ src, uint32_t n) {
+    for (uint32_t j = threadIdx.x; j < n; j += 4 * blockDim.x) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t jj = j + u * blockDim.x;
+            if (jj < n) v[u] = src[jj];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t jj = j + u * blockDim.x;
+            if (jj < n) dst[jj] = v[u];
+        }
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);

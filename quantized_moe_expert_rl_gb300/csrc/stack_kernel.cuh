@@ -553,9 +553,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             for (int k = 0; k < a.K; ++k) {
                 if (!((fm >> k) & 1u) || lo >= hi) continue;
                 const size_t at = (size_t)l * E + fid_s[k];
-                const uint4 *sp = reinterpret_cast<const uint4 *>(a.fill_src[at] + lo);
-                uint4 *dp = reinterpret_cast<uint4 *>(a.fill_dst[at] + lo);
-                for (size_t j = threadIdx.x; j < (hi - lo) / 16; j += kStThreads) dp[j] = sp[j];
+                copy16_batched(reinterpret_cast<uint4 *>(a.fill_dst[at] + lo),
+                               reinterpret_cast<const uint4 *>(a.fill_src[at] + lo), (uint32_t)((hi - lo) / 16));
             }
             if (!grid_sync(a.ctr, target, ok_s, a.ctrl, cap_grid)) { failed = true; break; }
             if (threadIdx.x < (unsigned)a.K && ((fm >> threadIdx.x) & 1u)) {

@@ -246,13 +246,15 @@ def run_reference(a):
         if i >= a.warmup:
             per_step.append(rate)
     value = sum(per_step) / len(per_step)
+    rate1, _, sample1 = oracle_rate(a.workload, budget_s=a.ref_step_s, cores=1)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": a.gpus,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000.0 * w.tokens / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config(w, a),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"per step: {sample}; ms_per_step is the time a whole step of "
-                                       f"{w.tokens} tokens takes at that rate"},
+                                       f"{w.tokens} tokens takes at that rate",
+                             "single_thread": {"value": rate1, "unit": "tokens/s", "cores": 1, "sample": sample1}},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -91,5 +91,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 3 and d["value"] > 0
     assert d["config"]["workload"] == "decode_stack" and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    st = d["cpu_baseline"]["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert abs(d["ms_per_step"] - 1000.0 * d["config"]["tokens_per_step"] / d["value"]) < 1e-6 * d["ms_per_step"]

@@ -58,7 +58,8 @@ def _tensor_peak():
 
 # The translation unit that holds each profiled kernel: its recorded DRAM traffic stays valid
 # while the code of that file and of every header it includes is unchanged.
-_KERNEL_TU = {"moe_decode_stack": "stack.cu", "moe_decode": "decode.cu", "tc_gemm": "prefill_tc.cu"}
+_KERNEL_TU = {"moe_decode_stack": "stack.cu", "moe_decode_layer": "stack.cu", "moe_decode": "decode.cu",
+              "tc_gemm": "prefill_tc.cu"}
 
 
 def _src_digest(kernel: str, root: str = ROOT) -> str:
@@ -267,8 +268,7 @@ def _config(w, a):
             "l2": "inputs larger than L2 (590.6 MB of weights per token)" if w.n_layers > 1 else
                   "per-token working set 12.3 MB (router stays L2-resident across tokens)",
             "parallelism": f"replicas x{a.gpus}", "seed": w.seed}
-    if w.n_layers > 1:
-        c["decode_path"] = getattr(a, "decode_path", "fused")
+    c["decode_path"] = getattr(a, "decode_path", "fused")
     return c
 
 
@@ -303,12 +303,16 @@ def run_ours(a):
     y_out = torch.zeros_like(x_in)
     y_host = torch.empty_like(x_host).pin_memory()
     stream = torch.cuda.Stream(device=dev)
-    fused = stacked and a.decode_path == "fused"
+    fused = a.decode_path == "fused"
 
     if fused:
-        # one moe_decode_stack launch per token runs all layers (plus the copy of x into y)
+        # one launch per token: moe_decode_stack runs all layers (plus the copy of x into y);
+        # for one layer without residual, moe_decode_layer runs the router and the experts
         def token(t):
-            engine.enqueue_decode_token_fused(model, b, x_in[t], y_out[t], pregate=a.pregate)
+            if stacked:
+                engine.enqueue_decode_token_fused(model, b, x_in[t], y_out[t], pregate=a.pregate)
+            else:
+                engine.enqueue_decode_layer_fused(model, b, x_in[t], y_out[t])
         launches_per_token = 1
 
         def step():
@@ -372,7 +376,27 @@ def run_ours(a):
     peak, peak_kind = _peaks()
     per_layer_bytes = w.top_k * w.record_bytes + w.n_experts * w.hidden * 4 + 2 * w.hidden * 4
     kt_tokens = min(T, 16)
-    if fused:
+    if fused and not stacked:
+        # ---- dominant kernel: moe_decode_layer, one launch = router + experts of one token ----
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(kt_tokens)]
+        ybuf = torch.zeros(w.hidden, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            for rep in range(2):                  # first pass warms the code path
+                for t in range(kt_tokens):
+                    s_, e_ = evs[t]
+                    s_.record(stream)
+                    engine.enqueue_decode_layer_fused(model, b, x_in[t], ybuf)
+                    e_.record(stream)
+        stream.synchronize()
+        t_launch = float(np.mean([s_.elapsed_time(e_) for s_, e_ in evs])) * 1e-3
+        achieved = per_layer_bytes / t_launch / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": _traffic("moe_decode_layer", 1.0),
+                    "kernel": "moe_decode_layer (router + experts of one token per launch)",
+                    "bytes_per_launch": per_layer_bytes, "launch_us": t_launch * 1e6,
+                    "peak_source": f"{peak_kind} hbm_gbs"}
+    elif fused:
         # ---- dominant kernel: moe_decode_stack, one launch = one token through every layer ----
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(kt_tokens)]
@@ -550,7 +574,7 @@ def decode_layer_leg(dev, steps: int, warmup: int) -> dict:
     bytes_launch = w.top_k * w.record_bytes + w.n_experts * w.hidden * 4 + 2 * w.hidden * 4
     peak, peak_kind = _peaks()
     froof = {"bound": "hbm", "achieved": bytes_launch / t_launch / 1e9, "peak": peak, "unit": "GB/s",
-             "frac": bytes_launch / t_launch / 1e9 / peak, "traffic": None,
+             "frac": bytes_launch / t_launch / 1e9 / peak, "traffic": _traffic("moe_decode_layer", 1.0),
              "kernel": "moe_decode_layer (router + experts of one token, one launch)",
              "bytes_per_launch": bytes_launch, "launch_us": t_launch * 1e6, "peak_source": f"{peak_kind} hbm_gbs"}
     return {"workload": "decode_layer (1 layer, 1000 tokens one at a time)",
@@ -767,8 +791,9 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-bounded", action="store_true")
     ap.add_argument("--decode-path", choices=["fused", "chain"], default="fused",
-                    help="stacked decode: one moe_decode_stack launch per token, or per-token graphs of the "
-                         "per-layer rl_route + moe_decode chain")
+                    help="one fused launch per token (moe_decode_stack through every layer; moe_decode_layer "
+                         "for the single-layer workload), or per-token graphs of the per-layer rl_route + "
+                         "moe_decode chain")
     ap.add_argument("--pregate", type=int, default=0,
                     help="fused decode: experts of the next layer prefetched into L2 on the pre-gated "
                          "prediction (0 = off)")

@@ -44,7 +44,7 @@ def test_digest_follows_the_translation_unit(tmp_path):
 
 def test_recorded_traffic_is_per_launch():
     d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-    for k in ("moe_decode_stack", "tc_gemm"):
+    for k in ("moe_decode_stack", "moe_decode_layer", "tc_gemm"):
         e = d[k]
         assert len(e["src_digest"]) == 16 and int(e["src_digest"], 16) >= 0
         # reported while the sources match the capture, else null (never a stale figure)

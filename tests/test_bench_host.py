@@ -22,7 +22,9 @@ def test_digest_follows_the_translation_unit(tmp_path):
     root, csrc = _tree(tmp_path)
     base = {k: bench._src_digest(k, root) for k in bench._KERNEL_TU}
     assert base == {k: bench._src_digest(k) for k in bench._KERNEL_TU}
-    assert len(set(base.values())) == len(base)
+    # one digest per translation unit: kernels built from the same unit share it
+    assert len(set(base.values())) == len(set(bench._KERNEL_TU.values()))
+    assert base["moe_decode_layer"] == base["moe_decode_stack"]
 
     # a comment-only change keeps every digest
     p = csrc / "stack_kernel.cuh"

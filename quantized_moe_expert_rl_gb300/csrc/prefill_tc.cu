@@ -18,6 +18,11 @@
 // f16 (the product of the f16 scale and the small integer needs up to 17 bits; f16 keeps 11),
 // the activations x and h are rounded to f16.  The f32 accumulator sees every K term.
 //
+// One thread issuing MMAs waits ~54 cycles per M = 128, K = 16 MMA whatever N (measured on
+// GB300), while at N = 16 the tensor pipe needs ~8: a unit of at most 64 tokens therefore has
+// two issuers, one per producer set, each summing its half of the K steps into an accumulator
+// of its own (the epilogue adds the two); a larger unit keeps the pipe busy with one issuer.
+//
 // Weights are the same for every token of a unit, so a heavy expert (many tokens, the Zipf
 // head of a skewed chunk) decodes its rows once per 128 tokens; the unit list puts the full
 // 128-token blocks first and the work is taken from a global counter, so the heavy units start
@@ -39,26 +44,35 @@ constexpr int kChunkV = 64;     // K values per B chunk (one 128-byte swizzle ro
 
 // warp roles
 constexpr int kTcProd = 8;                  // 0-7: A producers, two sets of four lane quadrants
-constexpr int kTcMmaW = 8;                  // MMA issuer (lane 0)
+constexpr int kTcMmaW = 8;                  // MMA issuer 0 (lane 0)
 constexpr int kTcRawW = 9;                  // unit fetch, pair metadata, bulk copy of the quantized rows
 constexpr int kTcBW = 10;                   // B tensor copies (lane 0)
 constexpr int kTcEpi0 = 11;                 // 11-14: epilogue, lane quadrants 3, 0, 1, 2
-constexpr int kTcWarps = 15;
+constexpr int kTcMma1W = 15;                // MMA issuer 1 (lane 0), on another SM sub-partition
+constexpr int kTcWarps = 16;
 constexpr int kTcThreads = kTcWarps * 32;
-constexpr int kRawArrivals = kTcProd + 1 + 1 + 4;  // every role that reads a unit's metadata
+constexpr int kMetaArrivals = 2 + 1 + 4;  // the roles that read a unit's metadata: issuers, B loader, epilogue
 
-// tensor memory: A stages at columns [0, 256) (64 columns each), accumulators at [256, 512)
+// tensor memory: A stages at columns [0, 256) (64 columns each), accumulators at [256, 512):
+// buffer b at 256 + 128 b, split into two 64-column halves (one per issuer) for units of at
+// most kSplitN tokens
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol0 = 256;
+constexpr int kSplitN = 64;
 
 // B stages of kNT rows x 128 bytes; a unit of npad tokens packs cps = 128 / npad chunks (a power
-// of two) into one stage, so that small units keep as many K values in flight as large ones
+// of two) into one stage, so that small units keep as many K values in flight as large ones.
+// (Measured: a fourth gate/up stage bought with a smaller codebook table, or more down stages,
+// did not make the chunk faster.)
 __host__ __device__ inline int tc_bstages(int MODE) { return MODE == 0 ? 3 : 6; }
 __host__ __device__ inline int tc_cps(int npad, int nchunks) {
     int c = 1;
     while (2 * c * npad <= kNT && 2 * c <= nchunks) c *= 2;
     return c;
 }
+// a unit's K steps are shared by the two issuers (step st by issuer st & 1) when it has at most
+// kSplitN tokens and at least two steps
+__host__ __device__ inline bool tc_split(int npad, int nsteps) { return npad <= kSplitN && nsteps >= 2; }
 // codebook as f16 pairs (exact: |value| <= 128), 8 interleaved copies (see qdot.cuh)
 __device__ void build_pair_table_f16(uint4 *tab, const int8_t *__restrict__ codebook) {
     for (int e = threadIdx.x; e < 256; e += blockDim.x) {
@@ -233,11 +247,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     extern __shared__ __align__(1024) uint8_t smem[];
     const PrefillArgs &a = args.a;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *raw_full = bars, *raw_empty = bars + 2, *a_full = bars + 4, *a_empty = bars + 8;
-    uint64_t *acc_full = bars + 12, *acc_empty = bars + 14, *fin_bar = bars + 16;
+    uint64_t *raw_full = bars, *meta_empty = bars + 2, *a_full = bars + 4, *a_empty = bars + 8;
+    uint64_t *acc_full = bars + 12, *acc_empty = bars + 14, *fin_bar = bars + 16, *meta_full = bars + 18;
+    uint64_t *data_empty = bars + 20;  // the quantized rows of a buffer decoded (producers)
     uint64_t *b_full = bars + 24, *b_empty = bars + 40;  // [sb] each, sb <= 16
     uint32_t *tmem_s = reinterpret_cast<uint32_t *>(smem + 512);
     int *abort_s = reinterpret_cast<int *>(smem + 516);
+    int *data_end = reinterpret_cast<int *>(smem + 520);  // [2]: no unit in this raw buffer
     const TcLayout lay(MODE, a.H, a.I);
     const int SB = lay.sb;
     uint4 *tab = reinterpret_cast<uint4 *>(smem + lay.o_tab);
@@ -253,18 +269,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kRawArrivals);
-            mbar_init(&acc_full[i], 1);
+            mbar_init(&meta_full[i], 1);
+            mbar_init(&meta_empty[i], kMetaArrivals);
+            mbar_init(&data_empty[i], kTcProd);
+            mbar_init(&acc_full[i], 2);  // one arrival per issuer
             mbar_init(&acc_empty[i], 4);
         }
         for (int i = 0; i < kAStages; ++i) {
             mbar_init(&a_full[i], 4);
             mbar_init(&a_empty[i], 1);
         }
-        mbar_init(fin_bar, 1);
+        mbar_init(fin_bar, 2);
         for (int i = 0; i < SB; ++i) {
             mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], 1);
+            mbar_init(&b_empty[i], 2);  // one arrival per issuer
         }
         *abort_s = 0;
         fence_mbar_init();
@@ -293,52 +311,71 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         if (!mbar_spin_warp(bar, parity)) fail_now();
         return !failed;
     };
-    // unit k's metadata (raw_full of its buffer); NULL at the end of the list or on failure
+    // unit k's metadata (meta_full of its buffer: published before its quantized rows land, so
+    // that the activations are requested while the weights are still on their way); NULL at the
+    // end of the list or on failure
     auto next_meta = [&](uint32_t k) -> const TcMeta * {
-        if (aborted() || !wait_spin(&raw_full[k & 1], (k >> 1) & 1)) return nullptr;
+        if (aborted() || !wait_spin(&meta_full[k & 1], (k >> 1) & 1)) return nullptr;
         const TcMeta *m = &meta[k & 1];
         return m->end ? nullptr : m;
     };
 
     if (warp == kTcRawW) {
         // ---------------- unit fetch + quantized rows ----------------
+        // Two buffers, each released twice: its quantized rows once the producers have decoded
+        // them (data_empty), its metadata once the issuers, the B loader and the epilogue are
+        // done with the unit (meta_empty).  So the next rows are requested while the epilogue
+        // still drains the unit before, and the metadata is published (meta_full) before the
+        // rows land, so that the activations are requested in the meantime.
+        // The next unit is claimed and its words, pairs and slot loaded while this one's
+        // buffers are awaited: that chain of dependent loads takes a few microseconds, as long as
+        // the producers take for a unit of the down GEMM.
         const size_t matb = matrix_bytes(a.I, a.H);
-        uint32_t k = 0;
-        for (;; ++k) {
-            const int rb = k & 1;
-            if (k >= 2 && (aborted() || !wait_spin(&raw_empty[rb], ((k >> 1) - 1) & 1))) break;
+        struct Unit {
+            bool end;
+            int e, mt, nvalid;
+            uint32_t p_lo, tok[kNT / 32];
+            uint8_t kk[kNT / 32];
+            uint64_t slot;  // lane 0
+        };
+        auto fetch = [&](Unit &f) {
             uint32_t u = 0;
             if (lane == 0) u = atomicAdd(&args.U.counts[2 + MODE], 1u);
             u = __shfl_sync(kFull, u, 0);
-            TcMeta &m = meta[rb];
-            if (u >= count) {
-                if (lane == 0) m.end = 1;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_full[rb]);
-                ++k;  // this buffer's phase completed without a copy
-                break;
-            }
+            f.end = u >= count;
+            f.e = f.mt = f.nvalid = 0;
+            f.p_lo = 0;
+            f.slot = 0;
+            if (f.end) return;
             const uint32_t uw = __ldcg(&units[u]);
-            const int e = uw & 1023, mt = (uw >> 10) & 31, tb = uw >> 15;
-            const uint32_t pe0 = __ldcg(&a.offs[e]), pe1 = __ldcg(&a.offs[e + 1]);
-            const uint32_t p_lo = pe0 + (uint32_t)tb * kNT;
-            const int nvalid = (int)min((uint32_t)kNT, pe1 - p_lo);
-            for (int i = lane; i < nvalid; i += 32) {
-                m.tok[i] = __ldcg(&a.pair_tok[p_lo + i]);
-                m.kk[i] = __ldcg(&a.pair_k[p_lo + i]);
+            f.e = uw & 1023;
+            f.mt = (uw >> 10) & 31;
+            const uint32_t pe0 = __ldcg(&a.offs[f.e]), pe1 = __ldcg(&a.offs[f.e + 1]);
+            f.p_lo = pe0 + (uw >> 15) * (uint32_t)kNT;
+            f.nvalid = (int)min((uint32_t)kNT, pe1 - f.p_lo);
+#pragma unroll
+            for (int i = 0; i < kNT / 32; ++i) {
+                const int n = lane + 32 * i;
+                f.tok[i] = n < f.nvalid ? __ldcg(&a.pair_tok[f.p_lo + n]) : 0u;
+                f.kk[i] = n < f.nvalid ? __ldcg(&a.pair_k[f.p_lo + n]) : (uint8_t)0;
             }
+            if (lane == 0) f.slot = __ldcg(&a.slots[(size_t)f.tok[0] * a.K + f.kk[0]]);
+        };
+        uint32_t armed = 0;  // units whose raw_full phase was started (a copy or a plain arrival)
+        // the quantized rows are read once per chunk: first out of L2, so that they do not push
+        // out the activations, which every row tile of an expert reads again
+        const uint64_t pol = l2_evict_first();
+        Unit cur, nxt;
+        fetch(cur);
+        for (uint32_t k = 0;; ++k) {
+            const int rb = k & 1;
+            if (k >= 2 && (aborted() || !wait_spin(&data_empty[rb], ((k >> 1) - 1) & 1))) break;
             if (lane == 0) {
-                m.end = 0;
-                m.e = e;
-                m.mt = mt;
-                m.nvalid = nvalid;
-                m.npad = (nvalid + 15) & ~15;
-                m.p_lo = p_lo;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                const uint64_t slot = __ldcg(&a.slots[(size_t)m.tok[0] * a.K + m.kk[0]]);
-                if (slot == 0 || (slot & 15)) {
+                data_end[rb] = cur.end ? 1 : 0;
+                const uint64_t slot = cur.slot;
+                if (cur.end) {
+                    mbar_arrive(&raw_full[rb]);
+                } else if (slot == 0 || (slot & 15)) {
                     // nothing is copied: the unit's outputs are garbage and the host sees the flag
                     dev_error(a.ctrl, slot == 0 ? RL_DEVERR_MISSING : RL_DEVERR_SLOT_ALIGN);
                     mbar_arrive(&raw_full[rb]);
@@ -347,24 +384,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                     uint8_t *dst = rawb + rb * lay.rawb;
                     if (MODE == 0) {
                         const uint32_t b = (uint32_t)matrix_bytes(kGuUnits, a.H);
-                        const uint8_t *g = rec + (size_t)mt * b;
+                        const uint8_t *g = rec + (size_t)cur.mt * b;
                         mbar_arrive_expect_tx(&raw_full[rb], 2 * b);
-                        bulk_g2s(dst, g, b, &raw_full[rb]);
-                        bulk_g2s(dst + b, g + matb, b, &raw_full[rb]);
+                        bulk_g2s_hint(dst, g, b, &raw_full[rb], pol);
+                        bulk_g2s_hint(dst + b, g + matb, b, &raw_full[rb], pol);
                     } else {
                         const uint32_t b = (uint32_t)matrix_bytes(kTcRows, a.I);
                         mbar_arrive_expect_tx(&raw_full[rb], b);
-                        bulk_g2s(dst, rec + 2 * matb + (size_t)mt * b, b, &raw_full[rb]);
+                        bulk_g2s_hint(dst, rec + 2 * matb + (size_t)cur.mt * b, b, &raw_full[rb], pol);
                     }
                 }
             }
+            armed = k + 1;
             __syncwarp();
+            if (!cur.end) fetch(nxt);
+            if (k >= 2 && (aborted() || !wait_spin(&meta_empty[rb], ((k >> 1) - 1) & 1))) break;
+            TcMeta &m = meta[rb];
+#pragma unroll
+            for (int i = 0; i < kNT / 32; ++i) {
+                const int n = lane + 32 * i;
+                if (n < cur.nvalid) {
+                    m.tok[n] = cur.tok[i];
+                    m.kk[n] = cur.kk[i];
+                }
+            }
+            if (lane == 0) {
+                m.end = cur.end ? 1 : 0;
+                m.e = cur.e;
+                m.mt = cur.mt;
+                m.nvalid = cur.nvalid;
+                m.npad = (cur.nvalid + 15) & ~15;
+                m.p_lo = cur.p_lo;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&meta_full[rb]);
+            __syncwarp();
+            if (cur.end) break;
+            cur = nxt;
         }
         // copies still in flight (only after a failure) must land before the CTA exits
-        for (uint32_t j = k >= 2 ? k - 2 : 0; j < k; ++j) mbar_wait_warp(&raw_full[j & 1], (j >> 1) & 1);
+        for (uint32_t j = armed >= 2 ? armed - 2 : 0; j < armed; ++j) mbar_wait_warp(&raw_full[j & 1], (j >> 1) & 1);
     } else if (warp == kTcBW) {
         // ---------------- B operand: tensor copies of the unit's activation rows ----------------
         uint32_t gbs = 0;  // B stages used so far
+        const uint64_t pol = l2_evict_last();
         for (uint32_t k = 0;; ++k) {
             const TcMeta *m = next_meta(k);
             if (!m) break;
@@ -377,15 +440,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                     mbar_arrive_expect_tx(&b_full[s], (uint32_t)(cps * npad * kChunkV * 2));
                     for (int j = 0; j < cps; ++j)
                         for (int r = 0; r < npad / 16; ++r)
-                            tma_load_2d(bst + ((size_t)s * kNT + j * npad + 16 * r) * (kChunkV * 2), &args.bmap,
-                                        (bs * cps + j) * kChunkV, (int)p_lo + 16 * r, &b_full[s]);
+                            tma_load_2d_hint(bst + ((size_t)s * kNT + j * npad + 16 * r) * (kChunkV * 2), &args.bmap,
+                                             (bs * cps + j) * kChunkV, (int)p_lo + 16 * r, &b_full[s], pol);
                 }
                 __syncwarp();
                 ++gbs;
             }
             if (failed) break;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&raw_empty[k & 1]);
+            if (lane == 0) mbar_arrive(&meta_empty[k & 1]);
         }
         // stages issued but never consumed (only after a failure) must land before the CTA exits
         for (uint32_t j = gbs >= (uint32_t)SB ? gbs - SB : 0; j < gbs; ++j) mbar_wait_warp(&b_full[j % SB], (j / SB) & 1);
@@ -402,8 +465,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         const uint32_t lanebase = tmem + ((uint32_t)(32 * q) << 16);
         uint32_t used = 0u, par = 0u;  // per stage: filled before; parity of its next fill
         for (uint32_t k = 0;; ++k) {
-            const TcMeta *m = next_meta(k);
-            if (!m) break;
+            // the producers need the unit's rows alone, not its metadata
+            if (aborted() || !wait_spin(&raw_full[k & 1], (k >> 1) & 1)) break;
+            if (*reinterpret_cast<volatile int *>(&data_end[k & 1])) break;
             const uint32_t raw = smem_addr(rawb + (k & 1) * lay.rawb);
             for (int st = J; st < nsteps; st += 2) {
                 const int sg = st % kAStages;
@@ -420,18 +484,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             }
             if (failed) break;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&raw_empty[k & 1]);
+            if (lane == 0) mbar_arrive(&data_empty[k & 1]);
         }
-    } else if (warp == kTcMmaW) {
-        // ---------------- MMA issuer: lane 0 alone ----------------
-        // Measured on GB300: one thread issues an M = 128, K = 16 MMA at best every ~45 cycles
-        // (the tensor pipe itself needs 64 cycles at N = 128 and 128 at N = 256, whatever the
-        // source of A), and every instruction the issuing thread adds around the MMAs slows the
-        // issue further.  At the ~10 pairs per expert of a 512-token chunk the grouped GEMM is
-        // bound by this issue rate, so the path is kept short: descriptors built once per B
-        // chunk and advanced by constants, a constant accumulate predicate after the unit's first
-        // K step, no warp-wide synchronisation.
+    } else if (warp == kTcMmaW || warp == kTcMma1W) {
+        // ---------------- MMA issuers: lane 0 of two warps ----------------
+        // Measured on GB300: one thread issues an M = 128, K = 16 MMA at best every ~54 cycles
+        // whatever N (the tensor pipe itself needs 64 cycles at N = 128), two threads issuing
+        // into separate accumulators twice as many.  So a unit of at most kSplitN tokens is
+        // shared: issuer I takes the K steps st with st & 1 == I (those of producer set I) into
+        // its own half of the accumulator buffer; a larger unit is issued by issuer 0 alone.
+        // Both issuers walk every step and every B stage of every unit, so that their stage
+        // parities stay in step with the fills; a B stage or an accumulator buffer is released
+        // by both (a commit where the issuer used it, a plain arrival where it did not).  The
+        // issue path is kept short: descriptors built once per B chunk and advanced by
+        // constants, no warp-wide synchronisation.
         if (lane == 0) {
+            const int me = warp == kTcMmaW ? 0 : 1;
             auto spin1 = [&](uint64_t *bar, uint32_t parity) {
                 for (uint32_t i = 0; i < kSpinPolls; ++i)
                     if (mbar_test_wait(bar, parity)) return true;
@@ -440,25 +508,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                 return false;
             };
             const uint32_t bst_s = tc::s_addr(bst);
-            uint32_t gbs = 0, par = 0u;  // B stages consumed; per A stage, parity of its next fill
+            uint32_t gbs = 0, par = 0u;  // B stages passed; per A stage, parity of its next fill
             for (uint32_t k = 0; !aborted(); ++k) {
-                if (!spin1(&raw_full[k & 1], (k >> 1) & 1)) break;
+                if (!spin1(&meta_full[k & 1], (k >> 1) & 1)) break;
                 const TcMeta *m = &meta[k & 1];
                 if (m->end) break;
                 const int npad = m->npad, cps = tc_cps(npad, nchunks);
+                const bool split = tc_split(npad, nsteps);
                 const uint32_t idesc = tc::instr_desc(0u, kTcRows, npad);
                 const uint32_t cstride = (uint32_t)(npad * kChunkV * 2);  // bytes between the chunks of a stage
-                mbar_arrive(&raw_empty[k & 1]);  // the metadata is no longer needed here
+                mbar_arrive(&meta_empty[k & 1]);  // the metadata is no longer needed here
                 const int ab = k & 1;
                 if (k >= 2 && !spin1(&acc_empty[ab], ((k >> 1) - 1) & 1)) break;
-                const uint32_t d = tmem + kAccCol0 + (uint32_t)(ab * kNT);
+                const uint32_t d = tmem + kAccCol0 + (uint32_t)(ab * kNT + (split ? me * kSplitN : 0));
                 int s = 0, j = 0;
                 uint32_t bc = 0;
+                bool first = true, stage_used = false;
                 for (int st = 0; st < nsteps; ++st) {
                     const int sg = st % kAStages;
-                    if (!spin1(&a_full[sg], (par >> sg) & 1u)) break;
+                    const bool mine = split ? (st & 1) == me : me == 0;
+                    if (mine) {
+                        if (!spin1(&a_full[sg], (par >> sg) & 1u)) break;
+                        tc::fence_after();
+                    }
                     par ^= 1u << sg;
-                    tc::fence_after();
                     const uint32_t a0 = tmem + (uint32_t)(sg * kStepV / 2);
 #pragma unroll
                     for (int c = 0; c < kStepV / kChunkV; ++c) {
@@ -468,27 +541,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                             tc::fence_after();
                             bc = bst_s + (uint32_t)(s * kNT * kChunkV * 2);
                         }
-                        const uint64_t bd = tc::smem_desc_sw128(bc, 1024);
-                        const uint32_t ac = a0 + (uint32_t)(c * kChunkV / 2);
-                        if (st == 0 && c == 0)
-                            tc::mma_f16_ts(d, ac, bd, idesc, 0u);
-                        else
-                            tc::mma_f16_ts_acc(d, ac, bd, idesc);
-                        tc::mma_f16_ts_acc(d, ac + 8, bd + 2, idesc);   // +32 bytes of B: start address field + 2
-                        tc::mma_f16_ts_acc(d, ac + 16, bd + 4, idesc);
-                        tc::mma_f16_ts_acc(d, ac + 24, bd + 6, idesc);
+                        if (mine) {
+                            const uint64_t bd = tc::smem_desc_sw128(bc, 1024);
+                            const uint32_t ac = a0 + (uint32_t)(c * kChunkV / 2);
+                            if (first)
+                                tc::mma_f16_ts(d, ac, bd, idesc, 0u);
+                            else
+                                tc::mma_f16_ts_acc(d, ac, bd, idesc);
+                            tc::mma_f16_ts_acc(d, ac + 8, bd + 2, idesc);   // +32 bytes of B: start address field + 2
+                            tc::mma_f16_ts_acc(d, ac + 16, bd + 4, idesc);
+                            tc::mma_f16_ts_acc(d, ac + 24, bd + 6, idesc);
+                            first = false;
+                            stage_used = true;
+                        }
                         bc += cstride;
                         if (++j == cps) {
-                            tc::commit(&b_empty[s]);
+                            if (stage_used)
+                                tc::commit(&b_empty[s]);
+                            else
+                                mbar_arrive(&b_empty[s]);
+                            stage_used = false;
                             ++gbs;
                             j = 0;
                         }
                     }
                     if (failed) break;
-                    tc::commit(&a_empty[sg]);
+                    if (mine) tc::commit(&a_empty[sg]);
                 }
                 if (failed) break;
-                tc::commit(&acc_full[ab]);
+                if (first)
+                    mbar_arrive(&acc_full[ab]);  // this issuer had no step of the unit
+                else
+                    tc::commit(&acc_full[ab]);
             }
         }
         __syncwarp();
@@ -503,10 +587,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             if (!wait_spin(&acc_full[ab], (k >> 1) & 1)) break;
             tc::fence_after();
             const int nvalid = m->nvalid, npad = m->npad, mt = m->mt;
+            const bool split = tc_split(npad, nsteps);
             const uint32_t p_lo = m->p_lo;
             for (int c0 = 0; c0 < npad; c0 += 16) {
                 uint32_t v[16];
                 tc::ld16(trow + (uint32_t)(ab * kNT + c0), v);
+                if (split) {  // the two issuers' partial sums, added in a fixed order
+                    uint32_t v1[16];
+                    tc::ld16(trow + (uint32_t)(ab * kNT + kSplitN + c0), v1);
+                    tc::ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                }
                 tc::ld_wait();
                 if (MODE == 0) {
                     // lane < 16: gate row of hidden unit hu, lane + 16: its up row.  The gate lane
@@ -537,17 +629,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&acc_empty[ab]);
-                mbar_arrive(&raw_empty[k & 1]);
+                mbar_arrive(&meta_empty[k & 1]);
             }
         }
     }
     if (failed && lane == 0) dev_error(a.ctrl, RL_DEVERR_WAIT_TIMEOUT);
     // drain every tcgen05 operation this CTA issued, then release tensor memory
     __syncthreads();
-    if (tid == kTcMmaW * 32) {
-        tc::commit(fin_bar);
-        if (!mbar_wait(fin_bar, 0)) dev_error(a.ctrl, RL_DEVERR_WAIT_TIMEOUT);  // the drain did not finish
-    }
+    if (tid == kTcMmaW * 32 || tid == kTcMma1W * 32) tc::commit(fin_bar);  // each issuer's own MMAs
+    if (tid == kTcMmaW * 32 && !mbar_wait(fin_bar, 0)) dev_error(a.ctrl, RL_DEVERR_WAIT_TIMEOUT);  // the drain did not finish
     tc::fence_before();
     __syncthreads();
     tc::fence_after();

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kR1Threads) route1_kernel(const float *__restr
 // ---------------------------------------------------------------------------------------------
 constexpr int kSgT = 128, kSgBK = 8, kSgPad = 4;
 
-__global__ void __launch_bounds__(256) router_sgemm_kernel(const float *__restrict__ xn, const float *__restrict__ W,
+__global__ void __launch_bounds__(256, 2) router_sgemm_kernel(const float *__restrict__ xn, const float *__restrict__ W,
                                                            const float *__restrict__ bias, float *__restrict__ out,
                                                            int T, int H, int E, int kslice, const int32_t *ctrl,
                                                            int layer) {
@@ -236,15 +236,16 @@ __global__ void resolve_slots_kernel(const int32_t *__restrict__ ids, const uint
 }
 
 constexpr int kSgMaxSplit = 8, kSgMaxSms = 256;
-// split-K factor of the many-token router GEMM: enough CTAs for `sms` SMs, K slices that stay
-// multiples of the K step.  The workspace is sized with kSgMaxSms, so it does not depend on the
-// device it was sized on.
+// split-K factor of the many-token router GEMM: enough CTAs for two per SM (two fit: 119
+// registers x 256 threads, 16.5 KB), K slices that stay multiples of the K step.  With one
+// 8-warp CTA per SM the FMA pipes wait on the shared-memory loads.  The workspace is sized with
+// kSgMaxSms, so it does not depend on the device it was sized on.
 static int router_splits(int T, int E, int H, int sms) {
     if (T <= 1) return 1;
     const int tiles = ((T + kSgT - 1) / kSgT) * ((E + kSgT - 1) / kSgT);
     sms = std::min(sms, kSgMaxSms);
     int S = 1;
-    while (S < kSgMaxSplit && tiles * S * 2 <= sms && H % (kSgBK * S * 2) == 0 && H / (S * 2) >= 64) S *= 2;
+    while (S < kSgMaxSplit && tiles * S * 2 <= 2 * sms && H % (kSgBK * S * 2) == 0 && H / (S * 2) >= 64) S *= 2;
     return S;
 }
 

@@ -43,6 +43,10 @@
 // RL_DEVERR_WAIT_TIMEOUT, waits (bounded) for its own copies in flight and returns; the other
 // CTAs then time out at their next barrier.
 #pragma once
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "decode_rows.cuh"
 #include "select.cuh"
 
@@ -820,25 +824,54 @@ static rl_status launch_stack(StackArgs a, cudaStream_t s) {
         kStWarps / a.K < 1)
         return fail(RL_ERR_UNSUPPORTED, "moe_decode_stack: shape does not fit one CTA per SM (H=%d E=%d K=%d I=%d)",
                     a.H, a.E, a.K, a.I);
-    // the router as a [n_layers * E][H] f32 matrix; a box is rc_rows(E) rows x dmax columns
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
-    if (!enc) return fail(RL_ERR_CUDA, "moe_decode_stack: cuTensorMapEncodeTiled unavailable");
-    const cuuint64_t gdim[2] = {(cuuint64_t)a.H, (cuuint64_t)a.n_layers * a.E};
-    const cuuint64_t gstride[1] = {(cuuint64_t)a.H * sizeof(float)};
-    const cuuint32_t box[2] = {(cuuint32_t)lay.dmax, (cuuint32_t)rc_rows(a.E)};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult cr = enc(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(a.W), gdim, gstride, box,
-                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS)
-        return fail(RL_ERR_UNSUPPORTED, "moe_decode_stack: router tensor map rejected (error %d, box %d x %d)", (int)cr,
-                    lay.dmax, rc_rows(a.E));
+    // The router as a [n_layers * E][H] f32 matrix; a box is rc_rows(E) rows x dmax columns.
+    // The encoded map and the occupancy check are kept per device and router (a single-layer
+    // launch is short enough that recomputing them on the host every time shows in the rate).
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int, int, int, int>, CUtensorMap> maps;  // every input of the map
+    static std::map<std::tuple<int, const void *, size_t>, int> occs;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(RL_ERR_CUDA, "moe_decode_stack: cudaGetDevice: %s", cudaGetErrorString(e));
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        const auto mk = std::make_tuple(dev, (const void *)a.W, a.H, a.E, a.n_layers, lay.dmax);
+        auto it = maps.find(mk);
+        if (it != maps.end()) {
+            a.wmap = it->second;
+        } else {
+            PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+            if (!enc) return fail(RL_ERR_CUDA, "moe_decode_stack: cuTensorMapEncodeTiled unavailable");
+            const cuuint64_t gdim[2] = {(cuuint64_t)a.H, (cuuint64_t)a.n_layers * a.E};
+            const cuuint64_t gstride[1] = {(cuuint64_t)a.H * sizeof(float)};
+            const cuuint32_t box[2] = {(cuuint32_t)lay.dmax, (cuuint32_t)rc_rows(a.E)};
+            const cuuint32_t estride[2] = {1, 1};
+            CUresult cr = enc(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(a.W), gdim, gstride, box,
+                              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (cr != CUDA_SUCCESS)
+                return fail(RL_ERR_UNSUPPORTED, "moe_decode_stack: router tensor map rejected (error %d, box %d x %d)",
+                            (int)cr, lay.dmax, rc_rows(a.E));
+            if (maps.size() >= 64) maps.clear();  // routers of models since freed
+            maps[mk] = a.wmap;
+        }
+    }
     rl_status st = allow_smem((const void *)kern, lay.total);
     if (st != RL_OK) return st;
     int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kStThreads, lay.total);
-    if (e != cudaSuccess || occ < 1)
-        return fail(RL_ERR_UNSUPPORTED, "moe_decode_stack: no SM can hold the %zu B CTA", lay.total);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        const auto ok = std::make_tuple(dev, (const void *)kern, lay.total);
+        auto it = occs.find(ok);
+        if (it != occs.end()) {
+            occ = it->second;
+        } else {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kStThreads, lay.total);
+            if (e != cudaSuccess) occ = 0;
+            else occs[ok] = occ;
+        }
+    }
+    if (occ < 1) return fail(RL_ERR_UNSUPPORTED, "moe_decode_stack: no SM can hold the %zu B CTA", lay.total);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(kStThreads);

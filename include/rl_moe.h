@@ -332,6 +332,9 @@ rl_status rl_build_pairs(const rl_moe_shape *shp, int32_t layer, int32_t T, cons
  * xn [T][H] f32; offs/pair_tok/pair_k from rl_build_pairs; slots uint64 [T][K] and weights
  * f32 [T][K] from rl_route; codebook int8 [256][8]; y [T][H] f32.  Skip when
  * ctrl[0] <= layer.  ws: moe_prefill_workspace_bytes(shp, T) bytes.
+ * Limit of this build: with inter = 2048 the down GEMM's shared-memory layout (six activation
+ * stages and two 66 KB weight buffers) exceeds the 227 KB a CTA may hold, and the call returns
+ * RL_ERR_CUDA from the attribute request before any launch.
  */
 size_t moe_prefill_workspace_bytes(const rl_moe_shape *shp, int32_t T);
 rl_status moe_prefill_chunk(const rl_moe_shape *shp, int32_t layer, int32_t T, const float *xn,

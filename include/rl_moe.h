@@ -260,6 +260,10 @@ rl_status moe_decode_static(const rl_moe_shape *shp, int32_t layer, const float 
  * makes CTA n-1 leave before its first grid-barrier arrival, and n < 0 makes CTA -n-1 expect
  * 16 bytes more than its first router-column copy brings, so that the other CTAs' waits run
  * out (RL_DEVERR_WAIT_TIMEOUT) without any fault; zero-fill ws again afterwards.
+ * Host side: the router's tensor-copy descriptor (built from the w_router address and the
+ * shape, never from its contents) and the occupancy check are computed once per device and
+ * kept, so repeated calls do no more host work than the launch; the launch may be captured in
+ * a CUDA graph.
  */
 size_t moe_decode_stack_workspace_bytes(const rl_moe_shape *shp);
 rl_status moe_decode_stack(const rl_moe_shape *shp, int32_t layer0, int32_t n_layers, float *x, float norm_eps,

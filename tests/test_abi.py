@@ -200,3 +200,58 @@ def test_selection_counts_beyond_the_index_range_are_refused(lib):
     assert lib.rl_fill_missing(ctypes.byref(s), 0, T, *([fake] * 8), fake, need, None) == RL_ERR_UNSUPPORTED
     for fn in (lib.moe_prefill_chunk, lib.moe_prefill_chunk_f32):
         assert fn(ctypes.byref(s), 0, T, *([fake] * 7), fake, 0, fake, fake, 1 << 62, None) == RL_ERR_UNSUPPORTED
+
+
+def test_prefill_host_checks(lib):
+    """moe_prefill_chunk and moe_prefill_chunk_f32: a layer out of range, a NULL per-token
+    buffer, a workspace too small and xn, y or ws off a 16-byte boundary are refused before any
+    launch (no GPU needed), with the reason in rl_last_error."""
+    from quantized_moe_expert_rl_gb300._lib import RL_ERR_INVALID, RlShape
+    s = RlShape.of(2048, 512, 10, 512, 48)
+    T = 512
+    need = lib.moe_prefill_workspace_bytes(ctypes.byref(s), T)
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+
+    def args(xn=fake, y=fake, ws=fake, ws_bytes=need, weights=fake):
+        # xn, offs, pair_tok, pair_k, slots, weights, codebook, y, accumulate, ctrl, ws, ws_bytes
+        return [xn, fake, fake, fake, fake, weights, fake, y, 0, fake, ws, ws_bytes, None]
+    for fn in (lib.moe_prefill_chunk, lib.moe_prefill_chunk_f32):
+        assert fn(ctypes.byref(s), 48, T, *args()) == RL_ERR_INVALID
+        assert b"layer" in lib.rl_last_error()
+        assert fn(ctypes.byref(s), -1, T, *args()) == RL_ERR_INVALID
+        assert fn(ctypes.byref(s), 0, -1, *args()) == RL_ERR_INVALID
+        assert fn(ctypes.byref(s), 0, T, *args(weights=None)) == RL_ERR_INVALID
+        assert b"NULL" in lib.rl_last_error()
+        assert fn(ctypes.byref(s), 0, T, *args(ws_bytes=need - 16)) == RL_ERR_INVALID
+        assert b"workspace" in lib.rl_last_error()
+        for bad in (dict(xn=odd), dict(y=odd), dict(ws=odd)):
+            assert fn(ctypes.byref(s), 0, T, *args(**bad)) == RL_ERR_INVALID, bad
+            assert b"aligned" in lib.rl_last_error()
+
+
+def test_pairs_and_slots_host_checks(lib):
+    """rl_build_pairs and rl_resolve_slots: a layer out of range, a negative T and a NULL
+    buffer are refused before any launch (no GPU needed)."""
+    from quantized_moe_expert_rl_gb300._lib import RL_ERR_INVALID, RlShape
+    s = RlShape.of(2048, 512, 10, 512, 48)
+    fake = ctypes.c_void_p(1 << 20)
+    # ids, offs, pair_tok, pair_k, ctrl
+    good = [fake] * 5
+    assert lib.rl_build_pairs(ctypes.byref(s), 48, 4, *good, None, 0, None) == RL_ERR_INVALID
+    assert b"layer" in lib.rl_last_error()
+    assert lib.rl_build_pairs(ctypes.byref(s), 0, -1, *good, None, 0, None) == RL_ERR_INVALID
+    for i in range(5):
+        bad = list(good)
+        bad[i] = None
+        assert lib.rl_build_pairs(ctypes.byref(s), 0, 4, *bad, None, 0, None) == RL_ERR_INVALID, i
+    # with no selections the per-selection buffers may be NULL, offs and ctrl may not
+    assert lib.rl_build_pairs(ctypes.byref(s), 0, 0, None, None, None, None, fake, None, 0, None) == RL_ERR_INVALID
+    assert lib.rl_build_pairs(ctypes.byref(s), 0, 0, None, fake, None, None, None, None, 0, None) == RL_ERR_INVALID
+    # ids, residency, slots
+    assert lib.rl_resolve_slots(ctypes.byref(s), 48, 4, fake, fake, fake, None) == RL_ERR_INVALID
+    assert lib.rl_resolve_slots(ctypes.byref(s), 0, -1, fake, fake, fake, None) == RL_ERR_INVALID
+    for i in range(3):
+        bad = [fake] * 3
+        bad[i] = None
+        assert lib.rl_resolve_slots(ctypes.byref(s), 0, 4, *bad, None) == RL_ERR_INVALID, i
